@@ -1,0 +1,14 @@
+"""fp64 CPU oracle for exact attention (test infrastructure only).
+
+Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline legs may
+import this package; the CUDA library never does.
+"""
+
+from .attention import (  # noqa: F401
+    attention_backward,
+    attention_decode,
+    attention_forward,
+    attention_forward_rows,
+    online_softmax_stats,
+    tiled_attention_row,
+)

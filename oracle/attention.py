@@ -1,0 +1,205 @@
+"""Plain, slow, fp64 CPU oracle for exact attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only the tests, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may call it.  It shares no code,
+table or constant with the CUDA library in ``exact_attention_84_gb300/csrc``.
+
+What it computes (sources are the four pages on FlashAttention; each
+function cites the passage it follows):
+
+* ``attention_forward``  -- the naive three-step definition
+  S = Q.K^T * scale, P = row-softmax(S) with the row maximum subtracted,
+  O = P.V, plus LSE = m + ln(l) per row.
+  ("03. FlashAttention", section "Le probleme", steps 1-3;
+  "FlashAttention ontleed", section "Het fysieke knelpunt"; the stored
+  statistic m, l from "Geheugencomplexiteit: van O(N^2) naar O(N)".)
+  FlashAttention is exact ("03. FlashAttention", "Benefices": "Exact";
+  Lensa ML "FlashAttention", step 6), so its oracle is this definition.
+* ``attention_backward`` -- the analytic gradient of O = softmax(S).V,
+  which the pages leave to "recompute P from the stored statistics"
+  ("03. FlashAttention", "Backward pass").  Written out by softmax
+  calculus: D_i = sum_k dO_ik O_ik, dV = P^T dO, dP = dO V^T,
+  dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+* ``attention_decode`` -- one query row per (batch, head) over the whole
+  KV cache, no mask ("FlashAttention ontleed", "Interactie met de
+  KV-cache"; Lensa ML FAQ on decoding).  It does NOT split the cache:
+  split-invariance is what the GPU path has to show.
+* ``online_softmax_stats`` and ``tiled_attention_row`` -- the pages'
+  running-max / running-sum recurrence, in the pages' order, used only to
+  pin the definition against the pages' worked example and exactness claim
+  (Lensa ML "FlashAttention", step 4 "Online Softmax" and step 6;
+  "FlashAttention ontleed", "Algoritmische kern in pseudocode").
+
+Readings taken where the pages are silent:
+* causal masking means key j is hidden from query i when j > i (square,
+  top-left aligned);
+* the stored statistic is one fp32 LSE = m + ln l in the natural log;
+* a row whose every score is masked does not occur under the square causal
+  mask (key 0 is always visible), so no special case is needed here.
+
+Every function takes numpy arrays of any float dtype and computes in
+float64.  Pins: tests/test_oracle.py.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "attention_forward",
+    "attention_forward_rows",
+    "attention_backward",
+    "attention_decode",
+    "online_softmax_stats",
+    "tiled_attention_row",
+]
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def _head_forward(q, k, v, scale, causal, rows):
+    """One head: q [Nq, d] (the query rows listed in ``rows``), k/v [Nk, d].
+
+    Step 1 of "Le probleme": S = Q.K^T (times scale, "FlashAttention
+    ontleed" pseudocode step 1 divides by sqrt(d)).  Step 2: the row softmax
+    with its maximum subtracted before exponentiation (Lensa ML step 4:
+    subtracting the maximum keeps the exponents small).  Step 3: O = P.V.
+    """
+    s = (q @ k.T) * scale                      # [Nq, Nk]
+    if causal:
+        cols = np.arange(k.shape[0])[None, :]
+        s = np.where(cols > np.asarray(rows)[:, None], -np.inf, s)
+    m = s.max(axis=1)                          # row maximum
+    e = np.exp(s - m[:, None])                 # exp(-inf) = 0 for masked keys
+    l = e.sum(axis=1)                          # row sum of exponentials
+    p = e / l[:, None]                         # P = softmax(S)
+    o = p @ v
+    lse = m + np.log(l)
+    return o, lse, p
+
+
+def attention_forward(q, k, v, scale: float, causal: bool):
+    """O = softmax(Q.K^T*scale [+ causal mask]).V and LSE for [..., N, d].
+
+    Leading dimensions (batch, heads) are looped over one head at a time.
+    Returns (O [..., N, d] float64, LSE [..., N] float64).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lead = q.shape[:-2]
+    n = q.shape[-2]
+    o = np.empty(q.shape[:-1] + (v.shape[-1],), dtype=np.float64)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    rows = np.arange(n)
+    for idx in np.ndindex(*lead):
+        o[idx], lse[idx], _ = _head_forward(q[idx], k[idx], v[idx], scale, causal, rows)
+    return o, lse
+
+
+def attention_forward_rows(q_rows, k, v, rows, scale: float, causal: bool):
+    """The same definition for a chosen subset of query rows of ONE head.
+
+    ``q_rows`` [R, d] are the query vectors at positions ``rows`` (needed for
+    the causal mask); ``k``, ``v`` [N, d] are the head's full key/value
+    matrices.  Each output row depends only on its own query row, so this is
+    the definition evaluated row by row, not a blocking of it.
+    """
+    o, lse, _ = _head_forward(_f64(q_rows), _f64(k), _f64(v), scale, causal,
+                              np.asarray(rows))
+    return o, lse
+
+
+def attention_backward(q, k, v, do, scale: float, causal: bool):
+    """Analytic gradients (dQ, dK, dV) of O = softmax(Q.K^T*scale).V.
+
+    P is recomputed from Q and K ("03. FlashAttention", "Backward pass":
+    only O and the softmax statistics are kept; P is recomputed).  Then, by
+    the chain rule through the row softmax:
+      dV = P^T dO
+      dP = dO V^T
+      D_i = sum_j P_ij dP_ij = sum_k dO_ik O_ik
+      dS = P * (dP - D)          (softmax Jacobian applied row by row)
+      dQ = scale * dS K,  dK = scale * dS^T Q
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    lead = q.shape[:-2]
+    n = q.shape[-2]
+    rows = np.arange(n)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    for idx in np.ndindex(*lead):
+        o, _, p = _head_forward(q[idx], k[idx], v[idx], scale, causal, rows)
+        g = do[idx]
+        dv[idx] = p.T @ g
+        dp = g @ v[idx].T
+        d_row = (g * o).sum(axis=1)
+        ds = p * (dp - d_row[:, None])
+        dq[idx] = scale * (ds @ k[idx])
+        dk[idx] = scale * (ds.T @ q[idx])
+    return dq, dk, dv
+
+
+def attention_decode(q, kcache, vcache, scale: float):
+    """One query token per (batch, head) against its whole KV cache.
+
+    q [..., d], kcache/vcache [..., L, d].  No mask: the new token sees every
+    cached position.  Returns (o [..., d], lse [...]).
+    """
+    q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+    lead = q.shape[:-1]
+    o = np.empty(lead + (vc.shape[-1],), dtype=np.float64)
+    lse = np.empty(lead, dtype=np.float64)
+    for idx in np.ndindex(*lead):
+        s = (kc[idx] @ q[idx]) * scale         # [L]
+        m = s.max()
+        e = np.exp(s - m)
+        l = e.sum()
+        o[idx] = (e @ vc[idx]) / l
+        lse[idx] = m + math.log(l)
+    return o, lse
+
+
+def online_softmax_stats(x, chunk: int):
+    """The pages' one-pass normaliser over a row of scores, chunk by chunk.
+
+    Lensa ML "FlashAttention", step 4: m_new = max(m, chunk max) and
+    l_new = l * e^(m - m_new) + sum e^(x - m_new), starting from m = -inf,
+    l = 0.  Returns the list of (m, l) after each chunk.
+    """
+    x = _f64(x)
+    m, l = -math.inf, 0.0
+    trace = []
+    for start in range(0, x.shape[0], chunk):
+        c = x[start:start + chunk]
+        m_new = max(m, float(c.max()))
+        l = l * math.exp(m - m_new) + float(np.exp(c - m_new).sum())
+        m = m_new
+        trace.append((m, l))
+    return trace
+
+
+def tiled_attention_row(q, k, v, scale: float, tile: int):
+    """One query row by the tiled loop of "FlashAttention ontleed",
+    section "Algoritmische kern in pseudocode": per K/V tile, the local
+    scores, the new running maximum, the rescaled exponentials, the output
+    rescaled by e^(m_old - m_new) and accumulated, and after the last tile a
+    single division by l.  Used only to pin the exactness claim of Lensa ML
+    step 6 (tiled equals standard up to rounding).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    m, l = -math.inf, 0.0
+    o = np.zeros(v.shape[-1], dtype=np.float64)
+    for start in range(0, k.shape[0], tile):
+        s = (k[start:start + tile] @ q) * scale
+        m_new = max(m, float(s.max()))
+        p = np.exp(s - m_new)
+        corr = math.exp(m - m_new)
+        l = corr * l + float(p.sum())
+        o = corr * o + p @ v[start:start + tile]
+        m = m_new
+    return o / l, m + math.log(l)

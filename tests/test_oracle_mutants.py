@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one (CPU only; the real oracle is never modified)."""
+
+import os
+import types
+
+import pytest
+
+from oracle_pins import ALL_PINS
+
+SRC = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "oracle", "attention.py")).read()
+
+MUTANTS = {
+    "transposed_scores": ("s = (q @ k.T) * scale",
+                          "s = ((q @ k.T).T if q.shape[0] == k.shape[0] else q @ k.T) * scale"),
+    "scale_divides": ("s = (q @ k.T) * scale", "s = (q @ k.T) / scale if scale else (q @ k.T)"),
+    "mask_includes_diagonal": ("cols > np.asarray(rows)[:, None]", "cols >= np.asarray(rows)[:, None]"),
+    "mask_hides_past": ("cols > np.asarray(rows)[:, None]", "cols < np.asarray(rows)[:, None]"),
+    "no_max_subtraction": ("e = np.exp(s - m[:, None])", "e = np.exp(s) * np.exp(0 * m[:, None])"),
+    "lse_drops_max": ("lse = m + np.log(l)", "lse = np.log(l)"),
+    "unnormalised_p": ("p = e / l[:, None]", "p = e"),
+    "dv_untransposed": ("dv[idx] = p.T @ g", "dv[idx] = p @ g"),
+    "ds_sign": ("ds = p * (dp - d_row[:, None])", "ds = p * (dp + d_row[:, None])"),
+    "ds_drops_d": ("ds = p * (dp - d_row[:, None])", "ds = p * dp"),
+    "dq_no_scale": ("dq[idx] = scale * (ds @ k[idx])", "dq[idx] = ds @ k[idx]"),
+    "dk_wrong_operand": ("dk[idx] = scale * (ds.T @ q[idx])", "dk[idx] = scale * (ds.T @ k[idx])"),
+    "dp_uses_k": ("dp = g @ v[idx].T", "dp = g @ k[idx].T"),
+    "decode_no_norm": ("o[idx] = (e @ vc[idx]) / l", "o[idx] = e @ vc[idx]"),
+    "decode_lse_no_max": ("lse[idx] = m + math.log(l)", "lse[idx] = math.log(l)"),
+    "online_no_rescale": ("l = l * math.exp(m - m_new) + float(np.exp(c - m_new).sum())",
+                          "l = l + float(np.exp(c - m_new).sum())"),
+    "tiled_no_out_rescale": ("o = corr * o + p @ v[start:start + tile]",
+                             "o = o + p @ v[start:start + tile]"),
+}
+
+
+def _load(src):
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src, "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    old, new = MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant = _load(SRC.replace(old, new))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, FloatingPointError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutant {name}"
