@@ -1,0 +1,88 @@
+"""Torch-facing convenience layer over the C-ABI.
+
+PyTorch only owns device memory and streams here: each function allocates
+its outputs with ``torch.empty`` and hands raw pointers to one C-ABI call on
+the current CUDA stream.  Inputs must be contiguous CUDA tensors of the
+documented dtype; nothing is converted or computed on the Python side.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O, LSE = attention(q, k, v) for [B, H, N, d] bf16 (or fp32) tensors."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    fp32 = q.dtype == torch.float32
+    dtype = torch.float32 if fp32 else torch.bfloat16
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, dtype, n)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    fn = _lib.fa_forward_fp32 if fp32 else _lib.fa_forward
+    _lib.check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                  B, H, N, d, scale, int(causal), _stream()))
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+             workspace=None):
+    """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
+            int(causal))
+    if workspace is None:
+        _lib.check(_lib.fa_backward(*args, _stream()))
+    else:
+        _lib.check(_lib.fa_backward_ex(*args, workspace.data_ptr(), workspace.numel() *
+                                       workspace.element_size(), _stream()))
+    return dq, dk, dv
+
+
+def decode(q, kcache, vcache, num_splits: int = 1, scale: float | None = None,
+           with_lse: bool = False, workspace=None):
+    """o (and optionally lse) for one query token per (b, h): q [B, H, d],
+    caches [B, H, Lkv, d], all bf16."""
+    B, H, L, d = kcache.shape
+    for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
+        _need(t, torch.bfloat16, n)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if with_lse else None
+    if scale is None and not with_lse and workspace is None:
+        _lib.check(_lib.fa_decode(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                  o.data_ptr(), B, H, L, d, num_splits, _stream()))
+    else:
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _lib.check(_lib.fa_decode_ex(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                     o.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                     B, H, L, d, num_splits, scale, ws_ptr, ws_bytes,
+                                     _stream()))
+    return (o, lse) if with_lse else o
+
+
+def device_status() -> int:
+    """Synchronise the current stream and return the kernels' status word."""
+    return _lib.fa_get_device_status(_stream())

@@ -1,0 +1,274 @@
+// api.cu -- the extern "C" boundary of libfa.so (declared in include/fa.h).
+//
+// Every entry point validates its arguments before anything is enqueued,
+// builds the TMA tensor maps it needs on the host, obtains workspace
+// (caller-owned, or stream-ordered cudaMallocAsync / cudaFreeAsync), and
+// launches the kernels of fwd_fp32.cu, fwd_bf16.cu, bwd_bf16.cu and
+// decode.cu on the caller's stream.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local fa::TimingEvents g_events;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled is a driver entry point; fetch it through the
+// runtime so the library does not link against libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [BH, N, 128] bf16 tensor; boxes of 64 columns (128 bytes,
+// the 128-byte swizzle span) by `box_rows` rows of one head.  Rows past N
+// read as zero.
+int make_map(CUtensorMap* map, const void* base, int BH, int N, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(N) * 128 * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return FA_OK;
+}
+
+int check_sizes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1)
+    return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d H=%d N=%d d=%d)", B, H, N, d);
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1ll << 30) || static_cast<long long>(N) > (1ll << 30))
+    return fail(FA_ERR_UNSUPPORTED, "B*H or N too large");
+  return FA_OK;
+}
+
+int check_scale(float scale) {
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", double(scale));
+  return FA_OK;
+}
+
+int launch_result(cudaError_t e, const char* what) {
+  if (e != cudaSuccess)
+    return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward: null pointer");
+  if (int r = check_sizes(B, H, N, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_forward: d must be 128 (got %d)", d);
+  if (int r = check_scale(scale)) return r;
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward: pointers must be 16-byte aligned");
+  fa::FwdMaps maps;
+  const int BH = B * H;
+  if (int r = make_map(&maps.q, q, BH, N, 128)) return r;
+  if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
+  if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
+  return launch_result(fa::launch_forward_bf16(maps, o, lse, B, H, N, scale, causal, stream, g_events),
+                       "fa_forward launch");
+}
+
+int fa_forward_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
+                    int B, int H, int N, int d, float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward_fp32: null pointer");
+  if (int r = check_sizes(B, H, N, d)) return r;
+  if (d % 32 != 0 || d > 128)
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp32: d must be 32, 64, 96 or 128 (got %d)", d);
+  if (int r = check_scale(scale)) return r;
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp32: pointers must be 16-byte aligned");
+  if (static_cast<long long>(N) > 65535ll * 16)
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp32: N too large");
+  if (static_cast<long long>(B) * H > 65535ll)
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp32: B*H must be <= 65535");
+  return launch_result(
+      fa::launch_forward_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, stream, g_events),
+      "fa_forward_fp32 launch");
+}
+
+static int backward_impl(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, void* ws,
+                         size_t ws_bytes, bool own_ws, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
+    return fail(FA_ERR_INVALID_ARG, "fa_backward: null pointer");
+  if (int r = check_sizes(B, H, N, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_backward: d must be 128 (got %d)", d);
+  if (int r = check_scale(scale)) return r;
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "fa_backward: pointers must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(lse) & 3u)
+    return fail(FA_ERR_INVALID_ARG, "fa_backward: lse must be 4-byte aligned");
+  const size_t need = fa::backward_workspace_bytes(B, H, N);
+  if (!own_ws) {
+    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+      return fail(FA_ERR_INVALID_ARG,
+                  "fa_backward_ex: workspace must be 256-byte aligned and >= %zu bytes", need);
+  }
+  const int BH = B * H;
+  fa::BwdMaps maps;
+  if (int r = make_map(&maps.q, q, BH, N, 64)) return r;
+  if (int r = make_map(&maps.dO, dO, BH, N, 64)) return r;
+  if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
+  if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
+  if (own_ws) {
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(FA_ERR_NO_MEMORY, "fa_backward: cudaMallocAsync of %zu bytes failed", need);
+    }
+  }
+  cudaError_t e = fa::launch_backward_bf16(maps, q, k, v, o, lse, dO, dq, dk, dv, B, H, N,
+                                           scale, causal, ws, stream, g_events);
+  if (own_ws) {
+    cudaError_t e2 = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  return launch_result(e, "fa_backward launch");
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, cudaStream_t stream) {
+  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, 0,
+                       true, stream);
+}
+
+int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H,
+                   int N, int d, float scale, int causal, void* ws, size_t ws_bytes,
+                   cudaStream_t stream) {
+  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, ws,
+                       ws_bytes, false, stream);
+}
+
+int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
+                 float* lse_out, int B, int H, int Lkv, int d, int num_splits, float scale,
+                 void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!q || !kcache || !vcache || !o) return fail(FA_ERR_INVALID_ARG, "fa_decode: null pointer");
+  if (int r = check_sizes(B, H, Lkv, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_decode: d must be 128 (got %d)", d);
+  if (int r = check_scale(scale)) return r;
+  if (num_splits < 1 || num_splits > Lkv || num_splits > 1024)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode: num_splits must be in [1, min(Lkv, 1024)] (got %d)",
+                num_splits);
+  if (static_cast<long long>(B) * H > 65535ll)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode: B*H must be <= 65535");
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode: pointers must be 16-byte aligned");
+  const size_t need = fa::decode_workspace_bytes(B, H, num_splits);
+  const bool own = (ws == nullptr);
+  if (!own && (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+    return fail(FA_ERR_INVALID_ARG,
+                "fa_decode_ex: workspace must be 256-byte aligned and >= %zu bytes", need);
+  if (own && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FA_ERR_NO_MEMORY, "fa_decode: cudaMallocAsync of %zu bytes failed", need);
+  }
+  cudaError_t e = fa::launch_decode(q, kcache, vcache, o, lse_out, B, H, Lkv, num_splits, scale,
+                                    ws, stream, g_events);
+  if (own) {
+    cudaError_t e2 = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  return launch_result(e, "fa_decode launch");
+}
+
+int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, int B, int H,
+              int Lkv, int d, int num_splits, cudaStream_t stream) {
+  const float scale = d > 0 ? 1.0f / std::sqrt(static_cast<float>(d)) : 1.0f;
+  return fa_decode_ex(q, kcache, vcache, o, nullptr, B, H, Lkv, d, num_splits, scale, nullptr,
+                      0, stream);
+}
+
+size_t fa_workspace_size(int op, int B, int H, int n_or_lkv, int d, int num_splits) {
+  if (B < 1 || H < 1 || n_or_lkv < 1 || d != 128) return 0;
+  switch (op) {
+    case FA_OP_FORWARD: return 0;
+    case FA_OP_BACKWARD: return fa::backward_workspace_bytes(B, H, n_or_lkv);
+    case FA_OP_DECODE:
+      if (num_splits < 1 || num_splits > n_or_lkv || num_splits > 1024) return 0;
+      return fa::decode_workspace_bytes(B, H, num_splits);
+    default: return 0;
+  }
+}
+
+int fa_get_device_status(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int s = 0;
+  const int parts[] = {fa::status_forward_fp32(true), fa::status_forward_bf16(true),
+                       fa::status_backward_bf16(true), fa::status_decode(true)};
+  for (int p : parts)
+    if (p != 0) s = p;
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (s != 0) return fail(FA_ERR_TIMEOUT, "a kernel wait ran out of time");
+  return ok();
+}
+
+int fa_set_timing_events(cudaEvent_t before, cudaEvent_t after) {
+  if ((before == nullptr) != (after == nullptr))
+    return fail(FA_ERR_INVALID_ARG, "fa_set_timing_events: set both events or neither");
+  g_events.before = before;
+  g_events.after = after;
+  return ok();
+}
+
+const char* fa_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// fa_internal.h -- launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Each kernel file owns one device status word
+// (a timeout record) and exposes a host function that reads and clears it.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+// Optional events recorded around a call's main kernel (nullptr: none).
+struct TimingEvents {
+  cudaEvent_t before = nullptr;
+  cudaEvent_t after = nullptr;
+};
+
+// ---- fp32 SIMT forward (fwd_fp32.cu)
+cudaError_t launch_forward_fp32(const float* q, const float* k, const float* v, float* o,
+                                float* lse, int B, int H, int N, int d, float scale,
+                                int causal, cudaStream_t stream, const TimingEvents& ev);
+int status_forward_fp32(bool clear);
+
+// ---- bf16 tcgen05 forward (fwd_bf16.cu); tensor maps over [B*H, N, 128]
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
+                                int N, float scale, int causal, cudaStream_t stream,
+                                const TimingEvents& ev);
+int status_forward_bf16(bool clear);
+
+// ---- bf16 backward (bwd_bf16.cu)
+struct BwdMaps {
+  CUtensorMap q, k, v, dO;
+};
+size_t backward_workspace_bytes(int B, int H, int N);
+cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
+                                 const void* v, const void* o, const float* lse,
+                                 const void* dO, void* dq, void* dk, void* dv, int B, int H,
+                                 int N, float scale, int causal, void* ws,
+                                 cudaStream_t stream, const TimingEvents& ev);
+int status_backward_bf16(bool clear);
+
+// ---- split-KV decode (decode.cu)
+size_t decode_workspace_bytes(int B, int H, int num_splits);
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o,
+                          float* lse_out, int B, int H, int L, int num_splits, float scale,
+                          void* ws, cudaStream_t stream, const TimingEvents& ev);
+int status_decode(bool clear);
+
+// Round a byte count up to 256.
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace fa

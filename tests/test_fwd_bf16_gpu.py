@@ -1,0 +1,67 @@
+"""bf16 tcgen05 forward against the oracle (max 2e-2, mean 2e-3 on O; 1e-3 on LSE)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as orc
+from exact_attention_84_gb300 import _lib, api, inputs
+from gpu_common import (G_MAX, FP32_TOL, LSE_MAX, O_MAX, assert_close_bf16, guarded,
+                        guards_intact, np64, status_clean)  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+# ------------------------------------------------------------- bf16 forward
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 1, 128), (1, 2, 129), (2, 3, 300),
+                                   (1, 1, 640), (1, 2, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_forward_shapes(B, H, N, causal):
+    d = 128
+    q, k, v = inputs.attention_inputs(B, H, N, d, torch.bfloat16, 20 + N, "cuda")
+    scale = 1 / math.sqrt(d)
+    bo, o = guarded((B, H, N, d), torch.bfloat16)
+    bl, lse = guarded((B, H, N), torch.float32)
+    api.forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+    o_ref, lse_ref = orc.attention_forward(np64(q), np64(k), np64(v), scale, causal)
+    assert_close_bf16(o, lse, o_ref, lse_ref, f"N={N} causal={causal}")
+    assert guards_intact(bo) and guards_intact(bl)
+
+
+def test_bf16_forward_other_scale():
+    q, k, v = inputs.attention_inputs(1, 2, 256, 128, torch.bfloat16, 77, "cuda")
+    o, lse = api.forward(q, k, v, causal=True, scale=0.02)
+    o_ref, lse_ref = orc.attention_forward(np64(q), np64(k), np64(v), 0.02, True)
+    assert_close_bf16(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_forward_b4_h16_n2048(causal):
+    w = inputs.FWD_N2048
+    q, k, v = inputs.workload_inputs(w, "cuda")
+    scale = 1 / math.sqrt(w.d)
+    o, lse = api.forward(q, k, v, causal=causal, scale=scale)
+    o_ref, lse_ref = orc.attention_forward(np64(q), np64(k), np64(v), scale, causal)
+    assert_close_bf16(o, lse, o_ref, lse_ref, f"causal={causal}")
+
+
+def test_bf16_long_causal_n8192_sampled():
+    w = inputs.LONG_CAUSAL
+    q, k, v = inputs.workload_inputs(w, "cuda")
+    scale = 1 / math.sqrt(w.d)
+    o, lse = api.forward(q, k, v, causal=True, scale=scale)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(w.N - 64, w.N),
+                                     rng.choice(w.N, 256, replace=False)]))
+    for h in (0, 13, w.uniform_head):
+        kh, vh = np64(k[0, h]), np64(v[0, h])
+        o_ref, lse_ref = orc.attention_forward_rows(np64(q[0, h, rows]), kh, vh, rows, scale,
+                                                    True)
+        assert_close_bf16(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, f"head {h}")
+    # the uniform head: every visible key has the same weight
+    h = w.uniform_head
+    vh = np64(v[0, h])
+    mean_prefix = np.cumsum(vh, axis=0) / np.arange(1, w.N + 1)[:, None]
+    assert np.abs(np64(o[0, h]) - mean_prefix).max() <= O_MAX
+
+
