@@ -113,7 +113,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -153,6 +153,16 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- helpers
+def lib_event():
+    """A timing event the library can record: torch creates events lazily,
+    so record it once here to make its handle exist."""
+    import torch
+
+    e = torch.cuda.Event(enable_timing=True)
+    e.record()
+    return e
+
+
 def kernel_source_hash(name: str) -> str:
     p = os.path.join(ROOT, "exact_attention_84_gb300", "csrc", name)
     with open(p, "rb") as f:
@@ -239,7 +249,7 @@ def run_ours(args, dist: Dist):
     if api.device_status() != 0:
         raise RuntimeError("kernel timeout during warm-up: " + _lib.fa_last_error())
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[lib_event() for _ in range(4)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dist.local)
@@ -354,8 +364,7 @@ def measure_targets(args, dev, peaks, peak_src):
         for i in range(3 + iters):
             if do_flush:
                 flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
+            a, b = lib_event(), lib_event()
             _lib.check(_lib.fa_set_timing_events(a.cuda_event, b.cuda_event))
             call()
             _lib.check(_lib.fa_set_timing_events(None, None))
@@ -457,7 +466,7 @@ def run_reference(args, dist: Dist):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-targets", action="store_true", help="skip the per-kernel targets")
