@@ -235,6 +235,39 @@ int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, in
                       0, stream);
 }
 
+int fa_decode_noalloc(const void* q, const void* kcache, const void* vcache, void* o,
+                      float* lse_out, int B, int H, int Lkv, int d, int num_splits, float scale,
+                      cudaStream_t stream) {
+  if (!q || !kcache || !vcache || !o)
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_noalloc: null pointer");
+  if (int r = check_sizes(B, H, Lkv, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_decode_noalloc: d must be 128 (got %d)", d);
+  if (int r = check_scale(scale)) return r;
+  if (num_splits < 1 || num_splits > Lkv || num_splits > 1024)
+    return fail(FA_ERR_INVALID_ARG,
+                "fa_decode_noalloc: num_splits must be in [1, min(Lkv, 1024)] (got %d)", num_splits);
+  const long long parts = static_cast<long long>(B) * H * num_splits;
+  if (parts > static_cast<long long>(fa::kNoAllocMaxParts))
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_noalloc: B*H*num_splits = %lld exceeds the fixed scratch capacity "
+                "of %zu parts; use fewer splits or fa_decode_ex",
+                parts, fa::kNoAllocMaxParts);
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)))
+    return fail(FA_ERR_INVALID_ARG, "fa_decode_noalloc: pointers must be 16-byte aligned");
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = fa::decode_noalloc_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess)
+    return fail(FA_ERR_CUDA, "fa_decode_noalloc: scratch address lookup failed: %s",
+                cudaGetErrorString(e));
+  if (fa::decode_workspace_bytes(B, H, num_splits) > scratch_bytes)
+    return fail(FA_ERR_UNSUPPORTED, "fa_decode_noalloc: scratch too small for this call");
+  e = fa::launch_decode(q, kcache, vcache, o, lse_out, B, H, Lkv, num_splits, scale, scratch,
+                        stream, g_events);
+  return launch_result(e, "fa_decode_noalloc launch");
+}
+
 size_t fa_workspace_size(int op, int B, int H, int n_or_lkv, int d, int num_splits) {
   if (B < 1 || H < 1 || n_or_lkv < 1 || d != 128) return 0;
   switch (op) {

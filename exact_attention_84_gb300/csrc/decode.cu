@@ -15,6 +15,7 @@
 // rows of every chunk (lane = 4 head-dimension elements), so two blocks per
 // SM keep ~190 KiB of loads in flight.
 #include <cfloat>
+#include <mutex>
 
 #include "fa_device.cuh"
 #include "fa_internal.h"
@@ -251,6 +252,41 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
   decode_combine_kernel<<<dim3(BH), dim3(HD), 0, stream>>>(
       part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse_out, num_splits);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for fa_decode_noalloc.  The split kernel writes every part's
+// partial output and lse here (B * H * num_splits parts at most
+// kNoAllocMaxParts) before the combine kernel reads them, so nothing in it has
+// to start at zero.  Every GPU that loads this library holds the array (about
+// 8.5 MB) until the process exits.  All calls share it: calls that overlap on
+// the GPU race on its contents.
+constexpr size_t kNoAllocFloats = kNoAllocMaxParts * (HD + 1);
+static __device__ __align__(256) float g_decode_scratch[kNoAllocFloats];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the scratch array on the current device.  In host code
+// `g_decode_scratch` names a host-side stand-in, so the address a kernel may
+// use is looked up once per device (with that device current) and cached.
+cudaError_t decode_noalloc_scratch(void** out, size_t* bytes) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  *bytes = sizeof(g_decode_scratch);
+  return cudaSuccess;
 }
 
 int status_decode(bool clear) {

@@ -50,6 +50,12 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
                           void* ws, cudaStream_t stream, const TimingEvents& ev);
 int status_decode(bool clear);
 
+// Fixed device scratch of fa_decode_noalloc (decode.cu): room for
+// kNoAllocMaxParts = B * H * num_splits partial results.
+constexpr size_t kNoAllocMaxParts = 16384;
+constexpr int kMaxDevices = 64;
+cudaError_t decode_noalloc_scratch(void** out, size_t* bytes);
+
 // Round a byte count up to 256.
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 

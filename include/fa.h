@@ -164,6 +164,31 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
                  float scale, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * fa_decode_noalloc -- fa_decode_ex without any allocation.  The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory themselves or let a library do it, e.g. a plugin running
+ * inside a host framework that owns every byte of device memory, or a
+ * latency-critical loop in which a cudaMalloc could stall the device.  The
+ * caller still passes the inputs and outputs, exactly as for fa_decode_ex
+ * (lse_out may be NULL); the split partials go to a fixed scratch array
+ * that the library holds on every GPU that loads it (about 8.5 MB, until the
+ * process exits).
+ *
+ *   Limit: B * H * num_splits <= 16384 partial results; larger requests are
+ *   rejected with FA_ERR_UNSUPPORTED and a message, and nothing is launched.
+ *   The first call on a device looks up that device's scratch address
+ *   (with the device current); make that first call before any stream
+ *   capture.  All calls share the one scratch array and its contents persist
+ *   between calls (every partial is written before it is read, so nothing
+ *   needs clearing); calls whose work overlaps on the GPU race on it, so
+ *   order them on one stream or synchronise between them.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int fa_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                      void* o, float* lse_out, int B, int H, int Lkv, int d,
+                      int num_splits, float scale, cudaStream_t stream);
+
+/*
  * fa_workspace_size -- device workspace bytes needed by an operation.
  *   op           FA_OP_FORWARD (always 0), FA_OP_BACKWARD or FA_OP_DECODE.
  *   n_or_lkv     N for forward/backward, Lkv for decode.
