@@ -2,11 +2,11 @@
 //
 // Method ("FlashAttention ontleed", sections "Tiling en Online Softmax" and
 // "Algoritmische kern in pseudocode"; "03. FlashAttention", section
-// "FlashAttention v1", "Mecanisme"): one thread block keeps a 128-row block
-// Q_i on chip while 128-row K_j / V_j tiles stream past it.  Per tile:
-//   S = Q_i K_j^T                  (tensor cores, fp32 accumulator in TMEM)
-//   m_new = max(m, rowmax(S*scale)) (softmax warps, registers)
-//   P = exp(S*scale - m_new)        (bf16, written to shared memory)
+// "FlashAttention v1", "Mecanisme"): Q blocks stay on chip while K_j / V_j
+// tiles stream past them.  Per tile and Q block:
+//   S = Q K_j^T                      (tensor cores, fp32 accumulator in TMEM)
+//   m_new = max(m, rowmax(S*scale))  (softmax warps, registers)
+//   P = exp(S*scale - m_new)         (bf16, written back into TMEM)
 //   l = l e^(m - m_new) + rowsum(P)
 //   O = diag(e^(m - m_new)) O + P V_j   (rescale in TMEM, MMA accumulates)
 // and after the last tile O / l and LSE = m + ln(l) go to HBM once.  The
@@ -14,19 +14,28 @@
 // step 3: 0 B of S written).
 //
 // GB300 mapping (the pages' A100/H100 designs are prior art only):
-//   warp 0      TMA producer: Q once, then K_j and V_j into a 2-stage ring
-//               (128-byte swizzled boxes of 64 columns) under mbarriers.
-//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma from one
-//               thread: S_j into one of two TMEM score buffers, then
-//               O += P_{j-1} V_{j-1}; completion via tcgen05.commit.
-//   warps 2-5   softmax: each thread owns one row (TMEM lane), reads its
-//               128 scores, keeps m and l in registers, exponentiates with
-//               ex2 on log2(e)-prescaled values, rescales its O row in TMEM
-//               when its maximum moved, writes P (bf16) into a swizzled
-//               shared-memory tile for the P.V MMA, and runs the epilogue.
-// Causal: key tiles above the diagonal are skipped; only the diagonal tile
-// (and a ragged last tile) is masked element-wise.  Heavy (late) query
-// blocks are scheduled first.
+//   * One thread block owns two 128-row Q blocks (A and B) that share every
+//     K/V tile.  Tiles are 128 keys; TMA streams K_j and V_j (128-byte
+//     swizzled 64-column boxes) into a 4-slot shared-memory ring.
+//   * TMEM (512 columns): S_A, S_B (128 each) and O_A, O_B (128 each).  The
+//     softmax writes P as packed bf16 over the first 64 columns of its S
+//     buffer, and the P.V product takes P straight from TMEM (A operand in
+//     tensor memory), so only V is read from shared memory for it.
+//   * Warps 0-3 run the softmax of block A, warps 4-7 that of block B (one
+//     thread per row = TMEM lane); warp 8 issues TMA; warp 9 allocates TMEM
+//     and issues every tcgen05.mma from one thread, interleaving the two
+//     blocks: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... so one block's
+//     softmax overlaps the other block's products.
+//   * The arrival of S(j) implies PV(j-1) of the same block has completed
+//     (one thread issues them in order and tcgen05.commit tracks all earlier
+//     products), so the softmax may rescale O in TMEM right then.  A row's
+//     reference maximum is only raised when the new maximum exceeds it by
+//     more than 8 (log2 units); otherwise the old reference is kept and the
+//     exponentials stay below 2^8.  O / l and LSE = m + ln(l) use the same
+//     reference, so the result is unchanged while most O rescales are skipped.
+// Causal: key tiles above the diagonal are skipped; only diagonal tiles (and
+// a ragged last tile) are masked element-wise.  Heavy (late) Q blocks are
+// scheduled first.
 #include <cfloat>
 
 #include "fa_device.cuh"
@@ -37,55 +46,78 @@ namespace {
 
 __device__ int g_status_fwd_bf16;
 
-constexpr int BM = 128;                 // query rows per block (TMEM lanes)
+constexpr int BM = 128;                 // query rows per Q block (TMEM lanes)
 constexpr int BN = 128;                 // keys per tile
 constexpr int HD = 128;                 // head dimension
-constexpr int STAGES = 2;               // K/V ring depth
+constexpr int SLOTS = 4;                // K/V ring slots (each one 128x128 bf16 tile)
 constexpr uint32_t TILE_BYTES = BM * HD * 2;        // 32 KiB
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;     // 128 rows x 64 columns
 
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
-constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + TILE_BYTES;
+constexpr uint32_t OFF_QA = 0;
+constexpr uint32_t OFF_QB = OFF_QA + TILE_BYTES;
+constexpr uint32_t OFF_SLOT = OFF_QB + TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_SLOT + SLOTS * TILE_BYTES;
 // barrier indices
 constexpr int B_QFULL = 0;
-constexpr int B_KFULL = 1;                 // + stage
-constexpr int B_VFULL = B_KFULL + STAGES;  // + stage
-constexpr int B_EMPTY = B_VFULL + STAGES;  // + stage
-constexpr int B_SFULL = B_EMPTY + STAGES;  // + buffer (2)
-constexpr int B_SFREE = B_SFULL + 2;       // + buffer (2)
-constexpr int B_PFULL = B_SFREE + 2;
-constexpr int B_ODONE = B_PFULL + 1;
-constexpr int NBAR = B_ODONE + 1;
+constexpr int B_FULL = 1;                  // + slot
+constexpr int B_EMPTY = B_FULL + SLOTS;    // + slot
+constexpr int B_SFULL = B_EMPTY + SLOTS;   // + block (A = 0, B = 1)
+constexpr int B_PFULL = B_SFULL + 2;       // + block
+constexpr int B_ODONE = B_PFULL + 2;       // + block
+constexpr int NBAR = B_ODONE + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // slack for 1024-byte alignment
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256;
+constexpr uint32_t TM_S = 0;          // + 128 * block
+constexpr uint32_t TM_O = 256;        // + 128 * block
 
-constexpr int NTHREADS = 192;
-constexpr int SOFTMAX_WARPS = 4;
+constexpr int NTHREADS = 320;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
 
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 // S = Q K^T: A = Q (K-major), B = K tile (K-major), M = N = 128.
 constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
-// O += P V: A = P (K-major over keys), B = V tile, whose rows run along the
-// reduction (key) axis with d contiguous: MN-major.
+// O += P V: A = P (in TMEM), B = V tile, whose rows run along the reduction
+// (key) axis with d contiguous: MN-major.
 constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
   return base + OFF_BAR + 8u * static_cast<uint32_t>(i);
 }
 
-__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, float* out) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
+struct Ctx {
+  uint32_t sbase;
+  volatile int* abort;
+  __device__ bool wait(int bar, uint32_t parity) const {
+    return mbar_wait(bar_addr(sbase, bar), parity, abort, &g_status_fwd_bf16);
+  }
+};
+
+__device__ __forceinline__ void issue_s(const Ctx& c, uint32_t tmem, int blk, uint32_t kslot) {
+  const uint32_t q = c.sbase + (blk ? OFF_QB : OFF_QA);
+  const uint32_t k = c.sbase + OFF_SLOT + kslot * TILE_BYTES;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(r[i]);
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+    mma_ss(tmem + TM_S + 128 * blk, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024),
+           IDESC_S, kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(const Ctx& c, uint32_t tmem, int blk, uint32_t vslot,
+                                         bool first) {
+  const uint32_t v = c.sbase + OFF_SLOT + vslot * TILE_BYTES;
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    // P: 16 keys = 8 packed columns per step; V: 16 key rows = 2048 bytes.
+    mma_ts(tmem + TM_O + 128 * blk, tmem + TM_S + 128 * blk + kk * 8,
+           sdesc_sw128(v + kk * 2048, HALF_BYTES, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
+  }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -98,34 +130,35 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  const Ctx ctx{sbase, abort_flag};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int nq = (N + BM - 1) / BM;
+  const int npair = (N + 2 * BM - 1) / (2 * BM);
   const int nkv = (N + BN - 1) / BN;
-  const int tile = blockIdx.x;
-  const int qi = causal ? (nq - 1 - tile / BH) : (tile / BH);
-  const int bh = tile % BH;
-  const int nt = causal ? min(qi + 1, nkv) : nkv;
+  const int pair = causal ? (npair - 1 - static_cast<int>(blockIdx.x) / BH)
+                          : (static_cast<int>(blockIdx.x) / BH);
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // key tiles needed by Q block A (tile 2*pair) and B (tile 2*pair + 1)
+  const int ntA = causal ? min(2 * pair + 1, nkv) : nkv;
+  const int ntB = causal ? min(2 * pair + 2, nkv) : nkv;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(sbase, B_QFULL), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_addr(sbase, B_KFULL + s), 1);
-      mbar_init(bar_addr(sbase, B_VFULL + s), 1);
+    for (int s = 0; s < SLOTS; ++s) {
+      mbar_init(bar_addr(sbase, B_FULL + s), 1);
       mbar_init(bar_addr(sbase, B_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_addr(sbase, B_SFULL + b), 1);
-      mbar_init(bar_addr(sbase, B_SFREE + b), SOFTMAX_WARPS);
+      mbar_init(bar_addr(sbase, B_PFULL + b), 4);
+      mbar_init(bar_addr(sbase, B_ODONE + b), 1);
     }
-    mbar_init(bar_addr(sbase, B_PFULL), SOFTMAX_WARPS);
-    mbar_init(bar_addr(sbase, B_ODONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
@@ -134,120 +167,124 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       const uint32_t qf = bar_addr(sbase, B_QFULL);
-      mbar_arrive_expect_tx(qf, TILE_BYTES);
-      tma_load_3d(sbase + OFF_Q, &tmQ, qf, 0, qi * BM, bh);
-      tma_load_3d(sbase + OFF_Q + HALF_BYTES, &tmQ, qf, 64, qi * BM, bh);
-      for (int j = 0; j < nt; ++j) {
-        const int st = j % STAGES;
-        if (j >= STAGES &&
-            !mbar_wait(bar_addr(sbase, B_EMPTY + st), ((j / STAGES) - 1) & 1, abort_flag,
-                       &g_status_fwd_bf16))
-          break;
-        const uint32_t kf = bar_addr(sbase, B_KFULL + st);
-        const uint32_t vf = bar_addr(sbase, B_VFULL + st);
-        const uint32_t ks = sbase + OFF_K + st * TILE_BYTES;
-        const uint32_t vs = sbase + OFF_V + st * TILE_BYTES;
-        mbar_arrive_expect_tx(kf, TILE_BYTES);
-        tma_load_3d(ks, &tmK, kf, 0, j * BN, bh);
-        tma_load_3d(ks + HALF_BYTES, &tmK, kf, 64, j * BN, bh);
-        mbar_arrive_expect_tx(vf, TILE_BYTES);
-        tma_load_3d(vs, &tmV, vf, 0, j * BN, bh);
-        tma_load_3d(vs + HALF_BYTES, &tmV, vf, 64, j * BN, bh);
+      const int q0 = pair * 2 * BM;
+      mbar_arrive_expect_tx(qf, 2 * TILE_BYTES);
+      tma_load_3d(sbase + OFF_QA, &tmQ, qf, 0, q0, bh);
+      tma_load_3d(sbase + OFF_QA + HALF_BYTES, &tmQ, qf, 64, q0, bh);
+      tma_load_3d(sbase + OFF_QB, &tmQ, qf, 0, q0 + BM, bh);
+      tma_load_3d(sbase + OFF_QB + HALF_BYTES, &tmQ, qf, 64, q0 + BM, bh);
+      bool ok = true;
+      int cnt = 0;
+      for (int j = 0; j < ntB && ok; ++j) {
+        for (int which = 0; which < 2 && ok; ++which, ++cnt) {
+          const int slot = cnt % SLOTS;
+          if (cnt >= SLOTS && !ctx.wait(B_EMPTY + slot, ((cnt / SLOTS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_addr(sbase, B_FULL + slot);
+          const uint32_t dst = sbase + OFF_SLOT + slot * TILE_BYTES;
+          const CUtensorMap* map = which ? &tmV : &tmK;
+          mbar_arrive_expect_tx(fb, TILE_BYTES);
+          tma_load_3d(dst, map, fb, 0, j * BN, bh);
+          tma_load_3d(dst + HALF_BYTES, map, fb, 64, j * BN, bh);
+        }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait(bar_addr(sbase, B_QFULL), 0, abort_flag, &g_status_fwd_bf16);
-      auto issue_pv = [&](int t) -> bool {
-        const int st = t % STAGES;
-        if (!mbar_wait(bar_addr(sbase, B_PFULL), t & 1, abort_flag, &g_status_fwd_bf16))
-          return false;
-        if (!mbar_wait(bar_addr(sbase, B_VFULL + st), (t / STAGES) & 1, abort_flag,
-                       &g_status_fwd_bf16))
-          return false;
-        tc_fence_after();
-        const uint32_t vs = sbase + OFF_V + st * TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(sbase + OFF_P + (kk >> 2) * HALF_BYTES + (kk & 3) * 32,
-                                         16, 1024);
-          const uint64_t b = sdesc_sw128(vs + kk * 2048, HALF_BYTES, 1024);
-          mma_ss(tmem + TM_O, a, b, IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar_addr(sbase, B_ODONE));
-        mma_commit(bar_addr(sbase, B_EMPTY + st));
-        return true;
+      // K_j sits in slot (2j) % SLOTS, V_j in (2j+1) % SLOTS; the n-th fill of
+      // a slot completes phase n of its FULL barrier.
+      auto full_k = [&](int j) { return ctx.wait(B_FULL + (2 * j) % SLOTS, ((2 * j) / SLOTS) & 1); };
+      auto full_v = [&](int j) {
+        return ctx.wait(B_FULL + (2 * j + 1) % SLOTS, ((2 * j + 1) / SLOTS) & 1);
       };
+      bool ok = ctx.wait(B_QFULL, 0) && full_k(0);
       if (ok) {
         tc_fence_after();
-        for (int j = 0; j < nt && ok; ++j) {
-          const int st = j % STAGES;
-          const int b = j & 1;
-          if (!mbar_wait(bar_addr(sbase, B_KFULL + st), (j / STAGES) & 1, abort_flag,
-                         &g_status_fwd_bf16)) {
-            ok = false;
-            break;
-          }
-          if (j >= 2 && !mbar_wait(bar_addr(sbase, B_SFREE + b), ((j >> 1) - 1) & 1,
-                                   abort_flag, &g_status_fwd_bf16)) {
-            ok = false;
-            break;
-          }
+        issue_s(ctx, tmem, 0, 0);
+        mma_commit(bar_addr(sbase, B_SFULL + 0));
+        issue_s(ctx, tmem, 1, 0);
+        mma_commit(bar_addr(sbase, B_SFULL + 1));
+        mma_commit(bar_addr(sbase, B_EMPTY + 0));
+      }
+      for (int j = 0; j < ntB && ok; ++j) {
+        const int vslot = (2 * j + 1) % SLOTS;
+        const int kslot_next = (2 * j + 2) % SLOTS;
+        bool v_ready = false, k_next_ready = false;
+        if (j < ntA) {
+          ok = ctx.wait(B_PFULL + 0, j & 1) && full_v(j);
+          if (!ok) break;
+          v_ready = true;
           tc_fence_after();
-          const uint32_t ks = sbase + OFF_K + st * TILE_BYTES;
-          const uint32_t sd = tmem + (b ? TM_S1 : TM_S0);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            const uint64_t a = sdesc_sw128(sbase + OFF_Q + off, 16, 1024);
-            const uint64_t bd = sdesc_sw128(ks + off, 16, 1024);
-            mma_ss(sd, a, bd, IDESC_S, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar_addr(sbase, B_SFULL + b));
-          if (j >= 1 && !issue_pv(j - 1)) ok = false;
+          issue_pv(ctx, tmem, 0, vslot, j == 0);
+          if (j == ntA - 1) mma_commit(bar_addr(sbase, B_ODONE + 0));
         }
-        if (ok) issue_pv(nt - 1);
+        if (j + 1 < ntA) {
+          ok = full_k(j + 1);
+          if (!ok) break;
+          k_next_ready = true;
+          tc_fence_after();
+          issue_s(ctx, tmem, 0, kslot_next);
+          mma_commit(bar_addr(sbase, B_SFULL + 0));
+        }
+        ok = ctx.wait(B_PFULL + 1, j & 1) && (v_ready || full_v(j));
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(ctx, tmem, 1, vslot, j == 0);
+        mma_commit(bar_addr(sbase, B_EMPTY + vslot));
+        if (j == ntB - 1) mma_commit(bar_addr(sbase, B_ODONE + 1));
+        if (j + 1 < ntB) {
+          ok = k_next_ready || full_k(j + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(ctx, tmem, 1, kslot_next);
+          mma_commit(bar_addr(sbase, B_SFULL + 1));
+          mma_commit(bar_addr(sbase, B_EMPTY + kslot_next));
+        }
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    const int blk = warp >> 2;                    // 0: block A, 1: block B
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
-    const int row = quad * 32 + lane;             // row of the Q block
-    const int q_row = qi * BM + row;
+    const int row = quad * 32 + lane;             // row within the Q block
+    const int qt = 2 * pair + blk;                // Q tile index (128-row units)
+    const int q_row = qt * BM + row;
+    const int nt = blk ? ntB : ntA;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    float m = -INFINITY;                          // running max, log2 units
+    const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * blk;
+    const uint32_t o_addr = tmem + lane_addr + TM_O + 128 * blk;
+    float m = -INFINITY;                          // reference max, log2 units
     float l = 0.f;                                // running sum
     bool ok = true;
-    uint8_t* sP = smem + OFF_P;
 
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(bar_addr(sbase, B_SFULL + b), (j >> 1) & 1, abort_flag,
-                     &g_status_fwd_bf16)) {
+      if (!ctx.wait(B_SFULL + blk, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float s[BN];
-      const uint32_t sd = tmem + lane_addr + (b ? TM_S1 : TM_S0);
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32_sync(sd + c * 32, s + c * 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_SFREE + b));
-
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      }
       // mask: causal diagonal tile, or keys past the end of the sequence
-      const bool diag = causal && (j == qi);
+      const bool diag = causal && (j == qt);
       const bool ragged = (j == nkv - 1) && (N % BN != 0);
       if (diag || ragged) {
         const int lim = causal ? min(q_row, N - 1) : (N - 1);
@@ -258,73 +295,61 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * scale_log2);
-      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float corr = fast_exp2(m - m_ref);
+      mx *= scale_log2;
+      // Raise the reference max only when the new one exceeds it by more
+      // than the threshold (always on the first tile, where m = -inf).
+      float corr = 1.f;
+      if (mx > m + kRescaleThreshold) {
+        corr = fast_exp2(m - mx);                 // 0 on the first tile
+        m = mx;
+      }
+      const bool rescale_o = (j > 0) && __any_sync(0xffffffffu, corr != 1.f);
       float rs = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -m_ref));
-        const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -m_ref));
+        const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -m));
+        const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -m));
         rs += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
       l = l * corr + rs;
-      m = m_new;
-
-      if (j > 0) {
-        // O and the P buffer are in use by P_{j-1} V_{j-1} until it completes.
-        if (!mbar_wait(bar_addr(sbase, B_ODONE), (j - 1) & 1, abort_flag,
-                       &g_status_fwd_bf16)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
-          const uint32_t od = tmem + lane_addr + TM_O;
+      // P (packed bf16) over the first 64 columns of this block's S buffer
+      tmem_st32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      tmem_st32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+      if (rescale_o) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(od + c * 32, r);
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-            tmem_st32(od + c * 32, r);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+          tmem_st32(o_addr + c * 32, r);
         }
       }
-      // P row -> shared memory in the 128-byte-swizzled K-major layout
-#pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const uint32_t off = (ch >> 3) * HALF_BYTES + sw128_offset(row, ch & 7);
-        *reinterpret_cast<uint4*>(sP + off) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL));
+      if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL + blk));
     }
 
-    if (ok && mbar_wait(bar_addr(sbase, B_ODONE), (nt - 1) & 1, abort_flag,
-                        &g_status_fwd_bf16)) {
+    if (ok && ctx.wait(B_ODONE + blk, 0)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const uint32_t od = tmem + lane_addr + TM_O;
       __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
-        float acc[32];
-        tmem_ld32_sync(od + c * 32, acc);
+        uint32_t r[32];
+        tmem_ld32(o_addr + c * 32, r);
         if (q_row < N) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pack_bf16x2(acc[8 * i] * inv_l, acc[8 * i + 1] * inv_l),
-                                pack_bf16x2(acc[8 * i + 2] * inv_l, acc[8 * i + 3] * inv_l),
-                                pack_bf16x2(acc[8 * i + 4] * inv_l, acc[8 * i + 5] * inv_l),
-                                pack_bf16x2(acc[8 * i + 6] * inv_l, acc[8 * i + 7] * inv_l));
+            dst[i] = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * i]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
         }
       }
       if (LSE != nullptr && q_row < N)
@@ -334,7 +359,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -354,10 +379,10 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
     attr_set = true;
   }
   const int BH = B * H;
-  const int nq = (N + BM - 1) / BM;
+  const int npair = (N + 2 * BM - 1) / (2 * BM);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (ev.before) cudaEventRecord(ev.before, stream);
-  fwd_bf16_kernel<<<dim3(nq * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
+  fwd_bf16_kernel<<<dim3(npair * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
