@@ -18,6 +18,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "fa_status.h"
 
 namespace {
 
@@ -161,8 +162,8 @@ static int backward_impl(const void* q, const void* k, const void* v, const void
   }
   const int BH = B * H;
   fa::BwdMaps maps;
-  if (int r = make_map(&maps.q, q, BH, N, 64)) return r;
-  if (int r = make_map(&maps.dO, dO, BH, N, 64)) return r;
+  if (int r = make_map(&maps.q, q, BH, N, 128)) return r;
+  if (int r = make_map(&maps.dO, dO, BH, N, 128)) return r;
   if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
   if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
   if (own_ws) {
@@ -290,7 +291,8 @@ int fa_get_device_status(cudaStream_t stream) {
     if (p != 0) s = p;
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-  if (s != 0) return fail(FA_ERR_TIMEOUT, "a kernel wait ran out of time");
+  if (s == fa::kStatusTimeout) return fail(FA_ERR_TIMEOUT, "a kernel wait ran out of time");
+  if (s != 0) return fail(FA_ERR_CUDA, "a kernel failed its launch-layout self-check (code %d)", s);
   return ok();
 }
 

@@ -10,20 +10,27 @@
 //   dV = P^T dO,  dS = P * (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels:
-//   bwd_pre      D = rowsum(dO * O) (fp32) and zeroing of the fp32 dQ
-//                accumulator.
+//   bwd_pre      D = rowsum(dO * O) and LSE * log2(e), both padded per head
+//                to a multiple of 128 rows (so every block copy is aligned
+//                and in bounds), and zeroing of the fp32 dQ accumulator.
 //   bwd_main     one thread block per (b, h, 128-key block j).  K_j and V_j
-//                stay in shared memory; 64-row blocks Q_i, dO_i stream past
-//                in a 2-stage TMA ring.  Per block i the tensor cores form
-//                S^T = K_j Q_i^T and dP^T = V_j dO_i^T in TMEM; the softmax
-//                warps (one key row per thread) turn them into P^T and dS^T
-//                (bf16, swizzled shared memory); the tensor cores then add
-//                dV += P^T dO_i and dK += dS^T Q_i in TMEM and form
-//                dQ_i^T = K_j^T dS^T, which four writer warps add into the
-//                fp32 accumulator with atomics.  dK, dV leave TMEM once.
+//                stay in shared memory; 128-row blocks Q_i, dO_i (with their
+//                LSE and D) stream past in a 2-stage TMA ring.  Per block i:
+//                  S^T  = K_j Q_i^T   -> TMEM R0      (shared-memory operands)
+//                  dP^T = V_j dO_i^T  -> TMEM R1
+//                  softmax warps (key row = TMEM lane) form
+//                  P^T = exp2(S^T scale log2e - LSE log2e) and
+//                  dS^T = P^T (dP^T - D), write both as packed bf16 over the
+//                  R0 columns they were computed from, and dS^T also to
+//                  shared memory;
+//                  dV += P^T dO_i, dK += dS^T Q_i   (A operand from TMEM)
+//                  dQ_i^T = K_j^T dS^T -> TMEM R1  (both operands MN-major)
+//                and four writer warps add scale * dQ_i into the fp32
+//                accumulator with atomics (one warp instruction covers 128
+//                contiguous bytes).  dK and dV leave TMEM once.
 //   bwd_convert  dQ = bf16(accumulator).
-// Causal: query blocks entirely above the key block are skipped; the two
-// blocks that straddle the diagonal are masked element-wise.
+// Causal: query blocks entirely above the key block are skipped; the
+// diagonal block is masked element-wise.
 #include <cfloat>
 
 #include "fa_device.cuh"
@@ -36,84 +43,95 @@ __device__ int g_status_bwd;
 
 constexpr int HD = 128;
 constexpr int BKV = 128;                  // key rows per block (TMEM lanes)
-constexpr int BQ = 64;                    // query rows per streamed block
-constexpr uint32_t KV_TILE = BKV * HD * 2;        // 32 KiB
-constexpr uint32_t KV_HALF = KV_TILE / 2;         // 128 rows x 64 cols
-constexpr uint32_t Q_TILE = BQ * HD * 2;          // 16 KiB
-constexpr uint32_t Q_HALF = Q_TILE / 2;           // 64 rows x 64 cols
-constexpr uint32_t PT_TILE = BKV * BQ * 2;        // 16 KiB, [key][query] bf16
+constexpr int BQ = 128;                   // query rows per streamed block
+constexpr uint32_t TILE = 128 * HD * 2;   // 32 KiB
+constexpr uint32_t HALF = TILE / 2;       // 128 rows x 64 columns
+constexpr uint32_t STAT = BQ * 4;         // 512 B of LSE*log2e or D per block
 
 constexpr uint32_t OFF_K = 0;
-constexpr uint32_t OFF_V = OFF_K + KV_TILE;
-constexpr uint32_t OFF_Q = OFF_V + KV_TILE;          // 2 stages
-constexpr uint32_t OFF_DO = OFF_Q + 2 * Q_TILE;      // 2 stages
-constexpr uint32_t OFF_PT = OFF_DO + 2 * Q_TILE;
-constexpr uint32_t OFF_DST = OFF_PT + PT_TILE;
-constexpr uint32_t OFF_STAT = OFF_DST + PT_TILE;     // [2 buffers][LSE 64 | D 64] fp32
-constexpr uint32_t OFF_BAR = OFF_STAT + 2 * 2 * BQ * 4;
+constexpr uint32_t OFF_V = OFF_K + TILE;
+constexpr uint32_t OFF_STAGE = OFF_V + TILE;                 // 2 stages
+constexpr uint32_t ST_Q = 0, ST_DO = TILE, ST_LSE = 2 * TILE, ST_D = 2 * TILE + STAT;
+constexpr uint32_t STAGE_BYTES = 2 * TILE + 2 * STAT;        // 65 KiB (1024-aligned)
+constexpr uint32_t OFF_DS = OFF_STAGE + 2 * STAGE_BYTES;     // dS^T, [key][query] bf16
+constexpr uint32_t OFF_BAR = OFF_DS + TILE;
 constexpr int B_KVFULL = 0;
 constexpr int B_QFULL = 1;     // + stage
 constexpr int B_QEMPTY = 3;    // + stage
-constexpr int B_SFULL = 5;
-constexpr int B_SFREE = 6;
-constexpr int B_PFULL = 7;
-constexpr int B_PFREE = 8;
-constexpr int B_DQFULL = 9;
-constexpr int B_DQFREE = 10;
-constexpr int B_STAT = 11;     // + buffer: the 128 softmax threads staged LSE / D
-constexpr int NBAR = 13;
+constexpr int B_SFULL = 5;     // S^T and dP^T in TMEM
+constexpr int B_PFULL = 6;     // P^T, dS^T written (8 softmax warps)
+constexpr int B_DSFREE = 7;    // shared dS^T consumed by the dQ product
+constexpr int B_DQFULL = 8;
+constexpr int B_DQFREE = 9;    // 4 writer warps have read dQ^T
+constexpr int B_DONE = 10;     // every product of the block completed
+constexpr int NBAR = 11;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // base is 1024-aligned (checked)
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DQ = 128, TM_DV = 256, TM_DK = 384;
+constexpr uint32_t TM_R0 = 0, TM_R1 = 128, TM_DV = 256, TM_DK = 384;
 
-constexpr int NTHREADS = 320;   // 0 producer, 1 MMA, 2-5 softmax, 6-9 dQ writers
+constexpr int NTHREADS = 448;   // 0-7 softmax, 8-11 dQ writers, 12 producer, 13 MMA
+constexpr int WARP_TMA = 12;
+constexpr int WARP_MMA = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 64 queries.
+// S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 128 queries.
 constexpr uint32_t IDESC_ST = idesc_bf16(BKV, BQ, false, false);
-// dV += P^T dO_i, dK += dS^T Q_i: M = 128 keys, N = 128 (d), B MN-major.
+// dV += P^T dO_i, dK += dS^T Q_i: A in TMEM, B MN-major; M = 128 keys, N = d.
 constexpr uint32_t IDESC_DKV = idesc_bf16(BKV, HD, false, true);
-// dQ_i^T = K_j^T dS^T: M = 128 (d), N = 64 queries; both operands MN-major.
+// dQ_i^T = K_j^T dS^T: M = d, N = 128 queries; both operands MN-major.
 constexpr uint32_t IDESC_DQ = idesc_bf16(HD, BQ, true, true);
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
   return base + OFF_BAR + 8u * static_cast<uint32_t>(i);
 }
 
-__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, float* out) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(r[i]);
-}
-
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
+struct Ctx {
+  uint32_t sbase;
+  volatile int* abort;
+  __device__ bool wait(int bar, uint32_t parity) const {
+    return mbar_wait(bar_addr(sbase, bar), parity, abort, &g_status_bwd);
+  }
+};
+
 // ------------------------------------------------------------------ bwd_pre
-// One warp per row: D = sum_k dO_k O_k; the row of the dQ accumulator is
-// zeroed at the same time.
+// One warp per (padded) row: D = sum_k dO_k O_k and LSE * log2(e), zero past
+// the end of the sequence; the row of the dQ accumulator is zeroed too.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
-                                                      float* __restrict__ Dvec,
-                                                      float* __restrict__ dq_acc,
-                                                      size_t rows) {
-  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+                                                      const float* __restrict__ lse,
+                                                      float* __restrict__ d_pad,
+                                                      float* __restrict__ lse_pad,
+                                                      float* __restrict__ dq_acc, int N,
+                                                      int Npad, size_t padded_rows) {
+  const size_t prow = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint2 a = *reinterpret_cast<const uint2*>(o + row * HD + lane * 4);
-  const uint2 b = *reinterpret_cast<const uint2*>(dO + row * HD + lane * 4);
-  float s = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16);
-  s = fmaf(__uint_as_float(a.x & 0xffff0000u), __uint_as_float(b.x & 0xffff0000u), s);
-  s = fmaf(__uint_as_float(a.y << 16), __uint_as_float(b.y << 16), s);
-  s = fmaf(__uint_as_float(a.y & 0xffff0000u), __uint_as_float(b.y & 0xffff0000u), s);
+  if (prow >= padded_rows) return;
+  const size_t bh = prow / Npad;
+  const int n = static_cast<int>(prow % Npad);
+  float s = 0.f, l2 = 0.f;
+  if (n < N) {
+    const size_t row = bh * N + n;
+    const uint2 a = *reinterpret_cast<const uint2*>(o + row * HD + lane * 4);
+    const uint2 b = *reinterpret_cast<const uint2*>(dO + row * HD + lane * 4);
+    s = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16);
+    s = fmaf(__uint_as_float(a.x & 0xffff0000u), __uint_as_float(b.x & 0xffff0000u), s);
+    s = fmaf(__uint_as_float(a.y << 16), __uint_as_float(b.y << 16), s);
+    s = fmaf(__uint_as_float(a.y & 0xffff0000u), __uint_as_float(b.y & 0xffff0000u), s);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) Dvec[row] = s;
-  *reinterpret_cast<float4*>(dq_acc + row * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    l2 = lse[row] * kLog2e;
+    *reinterpret_cast<float4*>(dq_acc + row * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (lane == 0) {
+    d_pad[prow] = s;
+    lse_pad[prow] = l2;
+  }
 }
 
 // --------------------------------------------------------------- bwd_convert
@@ -130,23 +148,26 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                const float* __restrict__ LSE, const float* __restrict__ Dvec,
+                const float* __restrict__ lse_pad, const float* __restrict__ d_pad,
                 float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dK,
-                __nv_bfloat16* __restrict__ dV, int BH, int N, float scale, int causal) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+                __nv_bfloat16* __restrict__ dV, int BH, int N, int Npad, float scale,
+                int causal) {
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {           // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicExch(&g_status_bwd, kStatusLayout);
+    return;
+  }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  const Ctx ctx{sbase, abort_flag};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const int j = tile / BH;                  // key block (small j = most work when causal)
-  const int bh = tile % BH;
+  const int j = static_cast<int>(blockIdx.x) / BH;    // key block (small j = most work when causal)
+  const int bh = static_cast<int>(blockIdx.x) % BH;
   const int nqb = (N + BQ - 1) / BQ;
-  const int i0 = causal ? (j * BKV) / BQ : 0;
+  const int i0 = causal ? j : 0;
   const int nit = nqb - i0;
   const float scale_log2 = scale * kLog2e;
 
@@ -157,17 +178,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_QEMPTY + s), 1);
     }
     mbar_init(bar_addr(sbase, B_SFULL), 1);
-    mbar_init(bar_addr(sbase, B_SFREE), 4);
-    mbar_init(bar_addr(sbase, B_PFULL), 4);
-    mbar_init(bar_addr(sbase, B_PFREE), 1);
+    mbar_init(bar_addr(sbase, B_PFULL), 8);
+    mbar_init(bar_addr(sbase, B_DSFREE), 1);
     mbar_init(bar_addr(sbase, B_DQFULL), 1);
     mbar_init(bar_addr(sbase, B_DQFREE), 4);
-    mbar_init(bar_addr(sbase, B_STAT), 128);
-    mbar_init(bar_addr(sbase, B_STAT + 1), 128);
+    mbar_init(bar_addr(sbase, B_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
@@ -176,7 +195,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -184,182 +203,182 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
       const uint32_t kvf = bar_addr(sbase, B_KVFULL);
-      mbar_arrive_expect_tx(kvf, 2 * KV_TILE);
+      mbar_arrive_expect_tx(kvf, 2 * TILE);
       tma_load_3d(sbase + OFF_K, &tmK, kvf, 0, j * BKV, bh);
-      tma_load_3d(sbase + OFF_K + KV_HALF, &tmK, kvf, 64, j * BKV, bh);
+      tma_load_3d(sbase + OFF_K + HALF, &tmK, kvf, 64, j * BKV, bh);
       tma_load_3d(sbase + OFF_V, &tmV, kvf, 0, j * BKV, bh);
-      tma_load_3d(sbase + OFF_V + KV_HALF, &tmV, kvf, 64, j * BKV, bh);
+      tma_load_3d(sbase + OFF_V + HALF, &tmV, kvf, 64, j * BKV, bh);
       for (int it = 0; it < nit; ++it) {
         const int st = it & 1;
         const int qb = (i0 + it) * BQ;
-        if (it >= 2 && !mbar_wait(bar_addr(sbase, B_QEMPTY + st), ((it >> 1) - 1) & 1,
-                                  abort_flag, &g_status_bwd))
-          break;
+        if (it >= 2 && !ctx.wait(B_QEMPTY + st, ((it >> 1) - 1) & 1)) break;
         const uint32_t qf = bar_addr(sbase, B_QFULL + st);
-        mbar_arrive_expect_tx(qf, 2 * Q_TILE);
-        const uint32_t qs = sbase + OFF_Q + st * Q_TILE;
-        const uint32_t ds = sbase + OFF_DO + st * Q_TILE;
-        tma_load_3d(qs, &tmQ, qf, 0, qb, bh);
-        tma_load_3d(qs + Q_HALF, &tmQ, qf, 64, qb, bh);
-        tma_load_3d(ds, &tmdO, qf, 0, qb, bh);
-        tma_load_3d(ds + Q_HALF, &tmdO, qf, 64, qb, bh);
+        const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
+        mbar_arrive_expect_tx(qf, 2 * TILE + 2 * STAT);
+        tma_load_3d(sb + ST_Q, &tmQ, qf, 0, qb, bh);
+        tma_load_3d(sb + ST_Q + HALF, &tmQ, qf, 64, qb, bh);
+        tma_load_3d(sb + ST_DO, &tmdO, qf, 0, qb, bh);
+        tma_load_3d(sb + ST_DO + HALF, &tmdO, qf, 64, qb, bh);
+        const size_t srow = static_cast<size_t>(bh) * Npad + qb;
+        bulk_load(sb + ST_LSE, lse_pad + srow, STAT, qf);
+        bulk_load(sb + ST_D, d_pad + srow, STAT, qf);
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = mbar_wait(bar_addr(sbase, B_KVFULL), 0, abort_flag, &g_status_bwd);
+      bool ok = ctx.wait(B_KVFULL, 0);
+      const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V, ds = sbase + OFF_DS;
       for (int it = 0; it < nit && ok; ++it) {
         const int st = it & 1;
-        const uint32_t qs = sbase + OFF_Q + st * Q_TILE;
-        const uint32_t ds = sbase + OFF_DO + st * Q_TILE;
-        ok = mbar_wait(bar_addr(sbase, B_QFULL + st), (it >> 1) & 1, abort_flag, &g_status_bwd);
-        if (ok && it > 0)
-          ok = mbar_wait(bar_addr(sbase, B_SFREE), (it - 1) & 1, abort_flag, &g_status_bwd);
+        const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
+        ok = ctx.wait(B_QFULL + st, (it >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
-        // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (reduction over d)
+        // S^T = K_j Q_i^T (reduction over d); R0 is free once the previous
+        // block's dV/dK products (issued earlier, executed in order) are done.
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * KV_HALF + (kk & 3) * 32;
-          const uint32_t kb = (kk >> 2) * Q_HALF + (kk & 3) * 32;
-          mma_ss(tmem + TM_S, sdesc_sw128(sbase + OFF_K + ka, 16, 1024),
-                 sdesc_sw128(qs + kb, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
-          mma_ss(tmem + TM_DP, sdesc_sw128(sbase + OFF_V + ka, 16, 1024),
-                 sdesc_sw128(ds + kb, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+          mma_ss(tmem + TM_R0, sdesc_sw128(kA + off, 16, 1024),
+                 sdesc_sw128(sb + ST_Q + off, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_addr(sbase, B_SFULL));
-        ok = mbar_wait(bar_addr(sbase, B_PFULL), it & 1, abort_flag, &g_status_bwd);
+        // dP^T = V_j dO_i^T into R1, once the writers have drained dQ^T.
+        if (it > 0) ok = ctx.wait(B_DQFREE, (it - 1) & 1);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO_i and dK += dS^T Q_i (reduction over the 64 queries)
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+          mma_ss(tmem + TM_R1, sdesc_sw128(vA + off, 16, 1024),
+                 sdesc_sw128(sb + ST_DO + off, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_addr(sbase, B_SFULL));
+        ok = ctx.wait(B_PFULL, it & 1);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO_i and dK += dS^T Q_i.  R0 holds, for each 32-query
+        // chunk g, P^T packed in columns [32g, 32g+16) and dS^T packed in
+        // [32g+16, 32g+32); a 16-query step is 8 packed columns.  dO_i, Q_i
+        // are MN-major B operands.
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ss(tmem + TM_DV, sdesc_sw128(sbase + OFF_PT + kk * 32, 16, 1024),
-                 sdesc_sw128(ds + kk * 2048, Q_HALF, 1024), IDESC_DKV, acc);
-          mma_ss(tmem + TM_DK, sdesc_sw128(sbase + OFF_DST + kk * 32, 16, 1024),
-                 sdesc_sw128(qs + kk * 2048, Q_HALF, 1024), IDESC_DKV, acc);
+          const uint32_t pcol = TM_R0 + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_ts(tmem + TM_DV, tmem + pcol, sdesc_sw128(sb + ST_DO + kk * 2048, HALF, 1024),
+                 IDESC_DKV, acc);
+          mma_ts(tmem + TM_DK, tmem + pcol + 16, sdesc_sw128(sb + ST_Q + kk * 2048, HALF, 1024),
+                 IDESC_DKV, acc);
         }
-        if (it > 0)
-          ok = mbar_wait(bar_addr(sbase, B_DQFREE), (it - 1) & 1, abort_flag, &g_status_bwd);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys)
+        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1.
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
-          mma_ss(tmem + TM_DQ, sdesc_sw128(sbase + OFF_K + kk * 2048, KV_HALF, 1024),
-                 sdesc_sw128(sbase + OFF_DST + kk * 2048, PT_TILE, 1024), IDESC_DQ,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + TM_R1, sdesc_sw128(kA + kk * 2048, HALF, 1024),
+                 sdesc_sw128(ds + kk * 2048, HALF, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_addr(sbase, B_DQFULL));
-        mma_commit(bar_addr(sbase, B_PFREE));
+        mma_commit(bar_addr(sbase, B_DSFREE));
         mma_commit(bar_addr(sbase, B_QEMPTY + st));
       }
+      if (ok) mma_commit(bar_addr(sbase, B_DONE));
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    const int half = warp >> 2;                       // query columns [64 half, 64 half + 64)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                 // key row within block j
     const int kv = j * BKV + row;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    const int gtid = threadIdx.x - 64;                // 0..127 within the group
-    float* stat = reinterpret_cast<float*>(smem + OFF_STAT);
+    uint8_t* ds_smem = smem + OFF_DS + half * HALF;
     bool ok = true;
-    for (int it = 0; it < nit; ++it) {
+    for (int it = 0; it < nit && ok; ++it) {
+      const int st = it & 1;
       const int qb = (i0 + it) * BQ;
-      float* st_buf = stat + (it & 1) * (2 * BQ);     // [LSE*log2e | D]
-      {
-        const int c = gtid & (BQ - 1);
-        const int q = qb + c;
-        float val = 0.f;
-        if (q < N) {
-          const size_t idx = static_cast<size_t>(bh) * N + q;
-          val = (gtid < BQ) ? LSE[idx] * kLog2e : Dvec[idx];
-        }
-        st_buf[gtid] = val;
-      }
-      // All 128 threads have staged their value before anyone reads the
-      // buffer; a buffer is rewritten two blocks later, after every thread
-      // has arrived here again (so has finished reading it).
-      mbar_arrive(bar_addr(sbase, B_STAT + (it & 1)));
-      if (!mbar_wait(bar_addr(sbase, B_STAT + (it & 1)), (it >> 1) & 1, abort_flag,
-                     &g_status_bwd) ||
-          !mbar_wait(bar_addr(sbase, B_SFULL), it & 1, abort_flag, &g_status_bwd)) {
+      const float* stage_lse =
+          reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
+      const float* stage_d =
+          reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_D);
+      // QFULL: the staged LSE / D are visible here; SFULL: S^T, dP^T in TMEM.
+      if (!ctx.wait(B_QFULL + st, (it >> 1) & 1) || !ctx.wait(B_SFULL, it & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[BQ], dp[BQ];
-      tmem_ld32_sync(tmem + lane_addr + TM_S, s);
-      tmem_ld32_sync(tmem + lane_addr + TM_S + 32, s + 32);
-      tmem_ld32_sync(tmem + lane_addr + TM_DP, dp);
-      tmem_ld32_sync(tmem + lane_addr + TM_DP + 32, dp + 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_SFREE));
-
-      const bool need_mask = (causal && qb < j * BKV + BKV) || (qb + BQ > N) || (kv >= N);
-      uint32_t pk[BQ / 2], dk[BQ / 2];
+      const bool need_mask = (causal && qb == j * BKV) || (qb + BQ > N) || (kv >= N);
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = half * 64 + c * 32;          // first query column of this chunk
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_addr + TM_R0 + col0, sr);
+        tmem_ld32(tmem + lane_addr + TM_R1 + col0, dr);
+        uint32_t pk[16], gk[16];
 #pragma unroll
-      for (int c = 0; c < BQ; c += 2) {
-        float p0 = fast_exp2(fmaf(s[c], scale_log2, -st_buf[c]));
-        float p1 = fast_exp2(fmaf(s[c + 1], scale_log2, -st_buf[c + 1]));
-        if (need_mask) {
-          const int q0 = qb + c;
-          if (q0 >= N || kv >= N || (causal && q0 < kv)) p0 = 0.f;
-          if (q0 + 1 >= N || kv >= N || (causal && q0 + 1 < kv)) p1 = 0.f;
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
+          const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], g[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            p[t] = fast_exp2(fmaf(__uint_as_float(sr[e + t]), scale_log2, -ls[t]));
+            if (need_mask) {
+              const int q = qb + col0 + e + t;
+              if (q >= N || kv >= N || (causal && q < kv)) p[t] = 0.f;
+            }
+            g[t] = p[t] * (__uint_as_float(dr[e + t]) - dd[t]);
+          }
+          pk[e / 2] = pack_bf16x2(p[0], p[1]);
+          pk[e / 2 + 1] = pack_bf16x2(p[2], p[3]);
+          gk[e / 2] = pack_bf16x2(g[0], g[1]);
+          gk[e / 2 + 1] = pack_bf16x2(g[2], g[3]);
         }
-        const float g0 = p0 * (dp[c] - st_buf[BQ + c]);
-        const float g1 = p1 * (dp[c + 1] - st_buf[BQ + c + 1]);
-        pk[c / 2] = pack_bf16x2(p0, p1);
-        dk[c / 2] = pack_bf16x2(g0, g1);
-      }
-      if (it > 0 && !mbar_wait(bar_addr(sbase, B_PFREE), (it - 1) & 1, abort_flag,
-                               &g_status_bwd)) {
-        ok = false;
-        break;
-      }
-      uint8_t* pt = smem + OFF_PT;
-      uint8_t* dst = smem + OFF_DST;
+        // Packed P^T and dS^T go over exactly the 32 columns this thread has
+        // just read (P^T first 16, dS^T last 16): no other warp reads them.
+        tmem_st16(tmem + lane_addr + TM_R0 + col0, pk);
+        tmem_st16(tmem + lane_addr + TM_R0 + col0 + 16, gk);
+        // dS^T row into shared memory (MN-major operand of the dQ product):
+        // the previous block's dQ product must have finished reading it.
+        if (c == 0 && it > 0 && !ctx.wait(B_DSFREE, (it - 1) & 1)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-      for (int ch = 0; ch < BQ / 8; ++ch) {
-        const uint32_t off = sw128_offset(row, ch);
-        *reinterpret_cast<uint4*>(pt + off) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(dst + off) =
-            make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t off = sw128_offset(row, c * 4 + ch);
+          *reinterpret_cast<uint4*>(ds_smem + off) =
+              make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
+        }
       }
+      if (!ok) break;
       fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL));
     }
-    // dK and dV rows leave TMEM once, after the last block's MMAs.
-    if (ok && nit > 0 &&
-        mbar_wait(bar_addr(sbase, B_PFREE), (nit - 1) & 1, abort_flag, &g_status_bwd)) {
+    // dV (warps 0-3) and dK (warps 4-7) leave TMEM once, after every product.
+    if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
       tc_fence_after();
+      __nv_bfloat16* out = half == 0 ? dV : dK;
+      const float mul = half == 0 ? 1.f : scale;
+      const uint32_t src = tmem + lane_addr + (half == 0 ? TM_DV : TM_DK);
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        __nv_bfloat16* out = half == 0 ? dV : dK;
-        const float mul = half == 0 ? 1.f : scale;
-        const uint32_t src = tmem + lane_addr + (half == 0 ? TM_DV : TM_DK);
-#pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          float acc[32];
-          tmem_ld32_sync(src + c * 32, acc);
-          if (kv < N) {
-            uint4* d4 = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + kv) * HD +
-                                                 c * 32);
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(src + c * 32, r);
+        if (kv < N) {
+          uint4* d4 =
+              reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + kv) * HD + c * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(pack_bf16x2(acc[8 * i] * mul, acc[8 * i + 1] * mul),
-                                 pack_bf16x2(acc[8 * i + 2] * mul, acc[8 * i + 3] * mul),
-                                 pack_bf16x2(acc[8 * i + 4] * mul, acc[8 * i + 5] * mul),
-                                 pack_bf16x2(acc[8 * i + 6] * mul, acc[8 * i + 7] * mul));
-          }
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * i]) * mul, __uint_as_float(r[8 * i + 1]) * mul),
+                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul),
+                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul),
+                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
         }
       }
     }
@@ -370,17 +389,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     for (int it = 0; it < nit; ++it) {
       const int qb = (i0 + it) * BQ;
-      if (!mbar_wait(bar_addr(sbase, B_DQFULL), it & 1, abort_flag, &g_status_bwd)) break;
+      if (!ctx.wait(B_DQFULL, it & 1)) break;
       tc_fence_after();
       float g[BQ];
-      tmem_ld32_sync(tmem + lane_addr + TM_DQ, g);
-      tmem_ld32_sync(tmem + lane_addr + TM_DQ + 32, g + 32);
+#pragma unroll
+      for (int c = 0; c < BQ / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + TM_R1 + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[c * 32 + i] = __uint_as_float(r[i]);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE));
       float* base = dq_acc + (static_cast<size_t>(bh) * N + qb) * HD + dcol;
       const int lim = min(BQ, N - qb);
-#pragma unroll 8
+#pragma unroll
       for (int c = 0; c < BQ; ++c)
         if (c < lim) red_add_f32(base + static_cast<size_t>(c) * HD, g[c] * scale);
     }
@@ -388,17 +412,20 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
+size_t padded_len(int N) { return (static_cast<size_t>(N) + BQ - 1) / BQ * BQ; }
+
 }  // namespace
 
 size_t backward_workspace_bytes(int B, int H, int N) {
   const size_t rows = static_cast<size_t>(B) * H * N;
-  return align256(rows * HD * sizeof(float)) + align256(rows * sizeof(float));
+  const size_t prow = static_cast<size_t>(B) * H * padded_len(N);
+  return align256(rows * HD * sizeof(float)) + 2 * align256(prow * sizeof(float));
 }
 
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
@@ -418,20 +445,24 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
     attr_set = true;
   }
   const int BH = B * H;
+  const int Npad = static_cast<int>(padded_len(N));
   const size_t rows = static_cast<size_t>(BH) * N;
+  const size_t prows = static_cast<size_t>(BH) * Npad;
   float* dq_acc = static_cast<float*>(ws);
-  float* Dvec = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                         align256(rows * HD * sizeof(float)));
-  bwd_pre_kernel<<<dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), Dvec, dq_acc,
-      rows);
+  float* d_pad = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                          align256(rows * HD * sizeof(float)));
+  float* lse_pad = reinterpret_cast<float*>(reinterpret_cast<char*>(d_pad) +
+                                            align256(prows * sizeof(float)));
+  bwd_pre_kernel<<<dim3(static_cast<unsigned>((prows + 7) / 8)), dim3(256), 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, d_pad,
+      lse_pad, dq_acc, N, Npad, prows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int nkv = (N + BKV - 1) / BKV;
   if (ev.before) cudaEventRecord(ev.before, stream);
   bwd_main_kernel<<<dim3(nkv * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
-      maps.q, maps.k, maps.v, maps.dO, lse, Dvec, dq_acc, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), BH, N, scale, causal);
+      maps.q, maps.k, maps.v, maps.dO, lse_pad, d_pad, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), BH, N, Npad, scale, causal);
   e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;
