@@ -26,7 +26,8 @@
 //                  dV += P^T dO_i, dK += dS^T Q_i   (A operand from TMEM)
 //                  dQ_i^T = K_j^T dS^T -> TMEM R1  (both operands MN-major)
 //                and four writer warps add scale * dQ_i into the fp32
-//                accumulator with atomics (one warp instruction covers 128
+//                accumulator with 16-byte vector atomics after a 4x4 register
+//                transpose (one warp instruction covers 4 rows x 128
 //                contiguous bytes).  dK and dV leave TMEM once.
 //   bwd_convert  dQ = bf16(accumulator).
 // Causal: query blocks entirely above the key block are skipped; the
@@ -74,6 +75,7 @@ constexpr uint32_t TM_R0 = 0, TM_R1 = 128, TM_DV = 256, TM_DK = 384;
 constexpr int NTHREADS = 448;   // 0-7 softmax, 8-11 dQ writers, 12 producer, 13 MMA
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
+constexpr int kHeadGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 128 queries.
@@ -87,8 +89,23 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
   return base + OFF_BAR + 8u * static_cast<uint32_t>(i);
 }
 
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+// Four consecutive fp32 values added atomically (16-byte aligned address).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+               ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// 4x4 transpose across each group of four lanes: on entry lane l holds
+// x[c] = its own value at position c; on exit it holds x[c] = the value that
+// lane (l & ~3) + c held at position (l & 3).
+__device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
+  const bool hi2 = lane & 2, hi1 = lane & 1;
+  float r0 = __shfl_xor_sync(0xffffffffu, hi2 ? x[0] : x[2], 2);
+  float r1 = __shfl_xor_sync(0xffffffffu, hi2 ? x[1] : x[3], 2);
+  if (hi2) { x[0] = r0; x[1] = r1; } else { x[2] = r0; x[3] = r1; }
+  r0 = __shfl_xor_sync(0xffffffffu, hi1 ? x[0] : x[1], 1);
+  r1 = __shfl_xor_sync(0xffffffffu, hi1 ? x[2] : x[3], 1);
+  if (hi1) { x[0] = r0; x[2] = r1; } else { x[1] = r0; x[3] = r1; }
 }
 
 struct Ctx {
@@ -164,9 +181,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int j = static_cast<int>(blockIdx.x) / BH;    // key block (small j = most work when causal)
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // Blocks are ordered by groups of kHeadGroup heads, so the few heads in
+  // flight keep their dQ accumulator, Q and dO resident in L2; within a
+  // group, key blocks go in increasing order (most work first when causal).
   const int nqb = (N + BQ - 1) / BQ;
+  const int nkv = (N + BKV - 1) / BKV;
+  const int per_group = kHeadGroup * nkv;
+  const int group = static_cast<int>(blockIdx.x) / per_group;
+  const int gsize = min(kHeadGroup, BH - group * kHeadGroup);
+  const int rem = static_cast<int>(blockIdx.x) - group * per_group;
+  const int j = rem / gsize;                          // key block
+  const int bh = group * kHeadGroup + rem % gsize;
   const int i0 = causal ? j : 0;
   const int nit = nqb - i0;
   const float scale_log2 = scale * kLog2e;
@@ -306,7 +331,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         break;
       }
       tc_fence_after();
-      const bool need_mask = (causal && qb == j * BKV) || (qb + BQ > N) || (kv >= N);
+      // Valid queries for this key row: q in [qlo, qhi] (causal: q >= kv;
+      // past the end of the sequence nothing is valid).  Applied as a select,
+      // no branch per element.
+      const int qlo = causal ? kv : 0;
+      const int qhi = kv < N ? N - 1 : -1;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         const int col0 = half * 64 + c * 32;          // first query column of this chunk
@@ -323,11 +352,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           float p[4], g[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
+            const int q = qb + col0 + e + t;
             p[t] = fast_exp2(fmaf(__uint_as_float(sr[e + t]), scale_log2, -ls[t]));
-            if (need_mask) {
-              const int q = qb + col0 + e + t;
-              if (q >= N || kv >= N || (causal && q < kv)) p[t] = 0.f;
-            }
+            p[t] = (q >= qlo && q <= qhi) ? p[t] : 0.f;
             g[t] = p[t] * (__uint_as_float(dr[e + t]) - dd[t]);
           }
           pk[e / 2] = pack_bf16x2(p[0], p[1]);
@@ -385,8 +412,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else {
     // ------------------------------------------------------------ dQ writers
     const int quad = warp & 3;
-    const int dcol = quad * 32 + lane;               // head-dimension index (TMEM lane)
-    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
     for (int it = 0; it < nit; ++it) {
       const int qb = (i0 + it) * BQ;
       if (!ctx.wait(B_DQFULL, it & 1)) break;
@@ -402,11 +428,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE));
-      float* base = dq_acc + (static_cast<size_t>(bh) * N + qb) * HD + dcol;
+      // Per group of 4 queries, transpose within each 4-lane group so that a
+      // lane holds 4 consecutive head-dimension values of one query row:
+      // one warp instruction then adds 4 rows x 128 contiguous bytes.
       const int lim = min(BQ, N - qb);
+      float* base = dq_acc + (static_cast<size_t>(bh) * N + qb + (lane & 3)) * HD +
+                    quad * 32 + (lane & ~3);
 #pragma unroll
-      for (int c = 0; c < BQ; ++c)
-        if (c < lim) red_add_f32(base + static_cast<size_t>(c) * HD, g[c] * scale);
+      for (int q0 = 0; q0 < BQ; q0 += 4) {
+        float x[4] = {g[q0] * scale, g[q0 + 1] * scale, g[q0 + 2] * scale, g[q0 + 3] * scale};
+        transpose4(x, lane);
+        if (q0 + (lane & 3) < lim)
+          red_add_v4(base + static_cast<size_t>(q0) * HD, x[0], x[1], x[2], x[3]);
+      }
     }
   }
 
