@@ -117,8 +117,10 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------ bwd_pre
-// One warp per (padded) row: D = sum_k dO_k O_k and LSE * log2(e), zero past
-// the end of the sequence; the row of the dQ accumulator is zeroed too.
+// Sixteen threads per (padded) row, 16 bytes each: D = sum_k dO_k O_k and
+// LSE * log2(e), zero past the end of the sequence; the row of the dQ
+// accumulator is zeroed too.  The padded row count is a multiple of 128, so
+// every warp covers two whole rows and every shuffle has all 32 lanes.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       const float* __restrict__ lse,
@@ -126,39 +128,46 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ lse_pad,
                                                       float* __restrict__ dq_acc, int N,
                                                       int Npad, size_t padded_rows) {
-  const size_t prow = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const size_t prow = static_cast<size_t>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int sub = threadIdx.x & 15;
   if (prow >= padded_rows) return;
   const size_t bh = prow / Npad;
   const int n = static_cast<int>(prow % Npad);
-  float s = 0.f, l2 = 0.f;
-  if (n < N) {
-    const size_t row = bh * N + n;
-    const uint2 a = *reinterpret_cast<const uint2*>(o + row * HD + lane * 4);
-    const uint2 b = *reinterpret_cast<const uint2*>(dO + row * HD + lane * 4);
-    s = __uint_as_float(a.x << 16) * __uint_as_float(b.x << 16);
-    s = fmaf(__uint_as_float(a.x & 0xffff0000u), __uint_as_float(b.x & 0xffff0000u), s);
-    s = fmaf(__uint_as_float(a.y << 16), __uint_as_float(b.y << 16), s);
-    s = fmaf(__uint_as_float(a.y & 0xffff0000u), __uint_as_float(b.y & 0xffff0000u), s);
+  const bool valid = n < N;
+  const size_t row = bh * N + n;
+  float s = 0.f;
+  if (valid) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * HD + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * HD + sub * 8);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    l2 = lse[row] * kLog2e;
-    *reinterpret_cast<float4*>(dq_acc + row * HD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 4; ++i) {
+      s = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), s);
+      s = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(bw[i] & 0xffff0000u), s);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + row * HD + sub * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (lane == 0) {
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (sub == 0) {
     d_pad[prow] = s;
-    lse_pad[prow] = l2;
+    lse_pad[prow] = valid ? lse[row] * kLog2e : 0.f;
   }
 }
 
 // --------------------------------------------------------------- bwd_convert
+// Eight accumulator values per thread -> one 16-byte bf16 store.
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restrict__ dq_acc,
                                                           __nv_bfloat16* __restrict__ dq,
-                                                          size_t n4) {
+                                                          size_t n8) {
   const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n4) return;
-  const float4 v = reinterpret_cast<const float4*>(dq_acc)[i];
-  reinterpret_cast<uint2*>(dq)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                               pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
 }
 
 // ------------------------------------------------------------------ bwd_main
@@ -487,7 +496,7 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
                                           align256(rows * HD * sizeof(float)));
   float* lse_pad = reinterpret_cast<float*>(reinterpret_cast<char*>(d_pad) +
                                             align256(prows * sizeof(float)));
-  bwd_pre_kernel<<<dim3(static_cast<unsigned>((prows + 7) / 8)), dim3(256), 0, stream>>>(
+  bwd_pre_kernel<<<dim3(static_cast<unsigned>((prows + 15) / 16)), dim3(256), 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, d_pad,
       lse_pad, dq_acc, N, Npad, prows);
   cudaError_t e = cudaGetLastError();
@@ -500,9 +509,9 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;
-  const size_t n4 = rows * HD / 4;
-  bwd_convert_kernel<<<dim3(static_cast<unsigned>((n4 + 255) / 256)), dim3(256), 0, stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), n4);
+  const size_t n8 = rows * HD / 8;
+  bwd_convert_kernel<<<dim3(static_cast<unsigned>((n8 + 255) / 256)), dim3(256), 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
   return cudaGetLastError();
 }
 
