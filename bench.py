@@ -270,34 +270,69 @@ def run_ours(args, dist: Dist):
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     value = (fwd_fl + bwd_fl) * dist.world / (ms_step * 1e-3) / 1e12
 
-    # --- end to end through the public API with host buffers
-    pin = [t.cpu().pin_memory() for t in (q, k, v, do)]
-    outs_h = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3)]
-    dq_api = [None]
+    # --- end to end through the public API with host buffers.  Every step
+    # copies its four inputs in from pinned host memory and its three
+    # gradients back out; as in a training loop, step i+1's upload and step
+    # i-1's download run on their own streams while step i computes
+    # (double-buffered device tensors, ordered by events).
+    pin_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    pin_out = [[torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3)]
+               for _ in range(2)]
+    dev_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
+    dev_o = [(torch.empty_like(q), torch.empty_like(lse)) for _ in range(2)]
+    dev_g = [[torch.empty_like(q) for _ in range(3)] for _ in range(2)]
+    s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        qd, kd, vd, dod = (h.to(dev, non_blocking=True) for h in pin)
-        od, lsed = api.forward(qd, kd, vd, causal=True, scale=scale)
-        g = api.backward(qd, kd, vd, od, lsed, dod, causal=True, scale=scale, workspace=ws)
-        for h, t in zip(outs_h, g):
-            h.copy_(t, non_blocking=True)
-        dq_api[0] = g[0]
+    def fresh_event():
+        e = torch.cuda.Event()
+        e.record()
+        return e
 
-    for _ in range(2):
-        e2e_step()
+    ev_in = [fresh_event() for _ in range(2)]
+    ev_used = [fresh_event() for _ in range(2)]
+    ev_out = [fresh_event() for _ in range(2)]
+
+    def e2e_step(i):
+        b = i % 2
+        with torch.cuda.stream(s_h2d):
+            s_h2d.wait_event(ev_used[b])        # step i-2 finished with these buffers
+            for d_, h_ in zip(dev_in[b], pin_in):
+                d_.copy_(h_, non_blocking=True)
+            ev_in[b].record(s_h2d)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[b])
+            s_comp.wait_event(ev_out[b])         # step i-2's gradients are on the host
+            qd, kd, vd, dod = dev_in[b]
+            od, lsed = api.forward(qd, kd, vd, causal=True, scale=scale, out=dev_o[b][0],
+                                   lse=dev_o[b][1])
+            api.backward(qd, kd, vd, od, lsed, dod, causal=True, scale=scale, workspace=ws,
+                         out=dev_g[b])
+            ev_used[b].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_used[b])
+            for h_, d_ in zip(pin_out[b], dev_g[b]):
+                h_.copy_(d_, non_blocking=True)
+            ev_out[b].record(s_d2h)
+
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     dist.barrier()
     e0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
+    for i in range(args.steps):
+        e2e_step(i)
     torch.cuda.synchronize()
     e2e_s = dist.max(time.perf_counter() - e0, dev) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in pin)
-    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    h2d = sum(t.numel() * t.element_size() for t in pin_in)
+    d2h = sum(t.numel() * t.element_size() for t in pin_out[0])
     e2e = {"value": round((fwd_fl + bwd_fl) * dist.world / e2e_s / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e2e_s * 1e3, 3)}
-    del pin, outs_h
+           "ms_per_step": round(e2e_s * 1e3, 3),
+           "overlap": "inputs in, compute, gradients out on three streams, double-buffered"}
+    # the last step's gradients came back through the host buffers: spot-check
+    if not torch.equal(pin_out[(args.steps - 1) % 2][0], dev_g[(args.steps - 1) % 2][0].cpu()):
+        raise RuntimeError("end-to-end gradients did not reach the host")
+    del pin_in, pin_out, dev_in, dev_o, dev_g
 
     # --- roofline of the dominant kernel (the backward dK/dV/dQ kernel)
     peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])

@@ -41,14 +41,20 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-             workspace=None):
-    """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``."""
+             workspace=None, out=None):
+    """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``.
+    ``out`` may hold three preallocated tensors (dq, dk, dv) to write into."""
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _need(t, torch.bfloat16, n)
     _need(lse, torch.float32, "lse")
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+        for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+            _need(t, torch.bfloat16, n)
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
             int(causal))

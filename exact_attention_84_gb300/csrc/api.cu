@@ -2,7 +2,7 @@
 //
 // Every entry point validates its arguments before anything is enqueued,
 // builds the TMA tensor maps it needs on the host, obtains workspace
-// (caller-owned, or stream-ordered cudaMallocAsync / cudaFreeAsync), and
+// (caller-owned, or from a library-owned stream-ordered pool), and
 // launches the kernels of fwd_fp32.cu, fwd_bf16.cu, bwd_bf16.cu and
 // decode.cu on the caller's stream.
 #include <cmath>
@@ -73,6 +73,39 @@ int make_map(CUtensorMap* map, const void* base, int BH, int N, int box_rows) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   return FA_OK;
+}
+
+// Workspace for calls made without one: a stream-ordered pool per device,
+// owned by the library, that keeps freed blocks for later calls (the default
+// pool returns them to the system at every synchronisation, which makes each
+// call pay for a fresh mapping).
+cudaError_t workspace_alloc(void** p, size_t bytes, cudaStream_t stream) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[fa::kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= fa::kMaxDevices) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (pools[dev] == nullptr) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&pools[dev], &props);
+      if (e != cudaSuccess) {
+        pools[dev] = nullptr;
+        return e;
+      }
+      uint64_t keep = ~static_cast<uint64_t>(0);
+      e = cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+      if (e != cudaSuccess) return e;
+    }
+    pool = pools[dev];
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pool, stream);
 }
 
 int check_sizes(int B, int H, int N, int d) {
@@ -167,9 +200,9 @@ static int backward_impl(const void* q, const void* k, const void* v, const void
   if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
   if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
   if (own_ws) {
-    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+    if (workspace_alloc(&ws, need, stream) != cudaSuccess) {
       cudaGetLastError();
-      return fail(FA_ERR_NO_MEMORY, "fa_backward: cudaMallocAsync of %zu bytes failed", need);
+      return fail(FA_ERR_NO_MEMORY, "fa_backward: workspace allocation of %zu bytes failed", need);
     }
   }
   cudaError_t e = fa::launch_backward_bf16(maps, q, k, v, o, lse, dO, dq, dk, dv, B, H, N,
@@ -216,9 +249,9 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
   if (!own && (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)))
     return fail(FA_ERR_INVALID_ARG,
                 "fa_decode_ex: workspace must be 256-byte aligned and >= %zu bytes", need);
-  if (own && cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+  if (own && workspace_alloc(&ws, need, stream) != cudaSuccess) {
     cudaGetLastError();
-    return fail(FA_ERR_NO_MEMORY, "fa_decode: cudaMallocAsync of %zu bytes failed", need);
+    return fail(FA_ERR_NO_MEMORY, "fa_decode: workspace allocation of %zu bytes failed", need);
   }
   cudaError_t e = fa::launch_decode(q, kcache, vcache, o, lse_out, B, H, Lkv, num_splits, scale,
                                     ws, stream, g_events);

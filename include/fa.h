@@ -108,9 +108,10 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o,
  *   dq, dk, dv      [B,H,N,d] bf16, written.
  *   d must be 128.  Other arguments as in fa_forward.
  * Workspace: fa_workspace_size(FA_OP_BACKWARD, ...) bytes (an fp32 dQ
- * accumulator and the D vector), taken with cudaMallocAsync on `stream`
- * and released with cudaFreeAsync on the same stream.  FA_ERR_NO_MEMORY if
- * that allocation fails.  dQ is summed with fp32 atomics: the result is not
+ * accumulator, D and a scaled copy of LSE), taken on `stream` from a
+ * stream-ordered memory pool the library keeps per device (freed blocks
+ * stay cached for later calls) and released on the same stream.
+ * FA_ERR_NO_MEMORY if that allocation fails.  dQ is summed with fp32 atomics: the result is not
  * bitwise reproducible from run to run (the pages accept summation-order
  * differences: "FlashAttention ontleed", "Beperkingen").
  */
@@ -146,7 +147,8 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
  *   d must be 128; 1 <= num_splits <= min(Lkv, 1024).  scale = 1/sqrt(d)
  *   (no scale argument; use fa_decode_ex for another one).
  * Workspace: fa_workspace_size(FA_OP_DECODE, ...) bytes of fp32 partials,
- * taken with cudaMallocAsync on `stream` and released with cudaFreeAsync.
+ * taken on `stream` from the library's per-device stream-ordered pool and
+ * released on the same stream.
  */
 int fa_decode(const void* q, const void* kcache, const void* vcache, void* o,
               int B, int H, int Lkv, int d, int num_splits,
