@@ -10,12 +10,13 @@
 //   dV = P^T dO,  dS = P * (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels:
-//   bwd_pre      D = rowsum(dO * O) and LSE * log2(e), both padded per head
+//   bwd_pre      -D = -rowsum(dO * O) and -LSE * log2(e), padded per head
 //                to a multiple of 128 rows (so every block copy is aligned
 //                and in bounds), and zeroing of the fp32 dQ accumulator.
 //   bwd_main     one thread block per (b, h, 128-key block j).  K_j and V_j
 //                stay in shared memory; 128-row blocks Q_i, dO_i (with their
-//                LSE and D) stream past in a 2-stage TMA ring.  Per block i:
+//                LSE and D) stream past in a 2-stage TMA ring.  Per block i,
+//                in two 64-query halves that overlap each other's softmax:
 //                  S^T  = K_j Q_i^T   -> TMEM R0      (shared-memory operands)
 //                  dP^T = V_j dO_i^T  -> TMEM R1
 //                  softmax warps (key row = TMEM lane) form
@@ -59,13 +60,13 @@ constexpr uint32_t OFF_BAR = OFF_DS + TILE;
 constexpr int B_KVFULL = 0;
 constexpr int B_QFULL = 1;     // + stage
 constexpr int B_QEMPTY = 3;    // + stage
-constexpr int B_SFULL = 5;     // S^T and dP^T in TMEM
-constexpr int B_PFULL = 6;     // P^T, dS^T written (8 softmax warps)
-constexpr int B_DSFREE = 7;    // shared dS^T consumed by the dQ product
-constexpr int B_DQFULL = 8;
-constexpr int B_DQFREE = 9;    // 4 writer warps have read dQ^T
-constexpr int B_DONE = 10;     // every product of the block completed
-constexpr int NBAR = 11;
+constexpr int B_SFULL = 5;     // + half: S^T and dP^T of 64 queries in TMEM
+constexpr int B_PFULL = 7;     // + half: their P^T, dS^T written (8 softmax warps)
+constexpr int B_DSFREE = 9;    // shared dS^T consumed by the dQ product
+constexpr int B_DQFULL = 10;
+constexpr int B_DQFREE = 11;   // 4 writer warps have read dQ^T
+constexpr int B_DONE = 12;     // every product of the block completed
+constexpr int NBAR = 13;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // base is 1024-aligned (checked)
 
@@ -78,8 +79,9 @@ constexpr int WARP_MMA = 13;
 constexpr int kHeadGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 128 queries.
-constexpr uint32_t IDESC_ST = idesc_bf16(BKV, BQ, false, false);
+// S^T = K_j Q_i^T and dP^T = V_j dO_i^T, one 64-query half at a time:
+// M = 128 keys, N = 64 queries.
+constexpr uint32_t IDESC_ST = idesc_bf16(BKV, BQ / 2, false, false);
 // dV += P^T dO_i, dK += dS^T Q_i: A in TMEM, B MN-major; M = 128 keys, N = d.
 constexpr uint32_t IDESC_DKV = idesc_bf16(BKV, HD, false, true);
 // dQ_i^T = K_j^T dS^T: M = d, N = 128 queries; both operands MN-major.
@@ -117,8 +119,8 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------ bwd_pre
-// Sixteen threads per (padded) row, 16 bytes each: D = sum_k dO_k O_k and
-// LSE * log2(e), zero past the end of the sequence; the row of the dQ
+// Sixteen threads per (padded) row, 16 bytes each: -D = -sum_k dO_k O_k and
+// -LSE * log2(e), zero past the end of the sequence; the row of the dQ
 // accumulator is zeroed too.  The padded row count is a multiple of 128, so
 // every warp covers two whole rows and every shuffle has all 32 lanes.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
@@ -151,9 +153,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (sub == 0) {
-    d_pad[prow] = s;
-    lse_pad[prow] = valid ? lse[row] * kLog2e : 0.f;
+  if (sub == 0) {            // stored negated: the main kernel only adds them
+    d_pad[prow] = -s;
+    lse_pad[prow] = valid ? -lse[row] * kLog2e : 0.f;
   }
 }
 
@@ -211,8 +213,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_QFULL + s), 1);
       mbar_init(bar_addr(sbase, B_QEMPTY + s), 1);
     }
-    mbar_init(bar_addr(sbase, B_SFULL), 1);
-    mbar_init(bar_addr(sbase, B_PFULL), 8);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar_addr(sbase, B_SFULL + h), 1);
+      mbar_init(bar_addr(sbase, B_PFULL + h), 8);
+    }
     mbar_init(bar_addr(sbase, B_DSFREE), 1);
     mbar_init(bar_addr(sbase, B_DQFULL), 1);
     mbar_init(bar_addr(sbase, B_DQFREE), 4);
@@ -261,43 +265,35 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
+    // Software-pipelined order, per query block i and 64-query half h:
+    //   ... dV0 dK0 | dQ^T(i) S0(i+1) dV1 dK1 | dP0(i+1) S1(i+1) dP1(i+1) | ...
+    // so half 0's softmax overlaps half 1's S/dP products, half 1's softmax
+    // overlaps dV0/dK0, and the writers drain dQ^T(i) while dV1/dK1 run.
     if (lane == 0) {
-      bool ok = ctx.wait(B_KVFULL, 0);
       const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V, ds = sbase + OFF_DS;
-      for (int it = 0; it < nit && ok; ++it) {
-        const int st = it & 1;
-        const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
-        ok = ctx.wait(B_QFULL + st, (it >> 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        // S^T = K_j Q_i^T (reduction over d); R0 is free once the previous
-        // block's dV/dK products (issued earlier, executed in order) are done.
+      auto stage = [&](int it) { return sbase + OFF_STAGE + (it & 1) * STAGE_BYTES; };
+      // S^T (into R0) or dP^T (into R1) for half h of block `it`: reduction
+      // over d; the half's 64 query rows start 64 * 128 bytes into each
+      // 64-column box of the Q / dO tile.
+      auto issue_sdp = [&](int it, int h, bool dp) {
+        const uint32_t a = dp ? vA : kA;
+        const uint32_t b = stage(it) + (dp ? ST_DO : ST_Q) + h * 64 * 128;
+        const uint32_t d = tmem + (dp ? TM_R1 : TM_R0) + h * 64;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_ss(tmem + TM_R0, sdesc_sw128(kA + off, 16, 1024),
-                 sdesc_sw128(sb + ST_Q + off, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
+          mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), IDESC_ST,
+                 kk > 0 ? 1u : 0u);
         }
-        // dP^T = V_j dO_i^T into R1, once the writers have drained dQ^T.
-        if (it > 0) ok = ctx.wait(B_DQFREE, (it - 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
+      };
+      // dV += P^T dO_i and dK += dS^T Q_i over the 64 queries of half h.  R0
+      // holds, per 32-query chunk g, P^T packed in columns [32g, 32g+16) and
+      // dS^T packed in [32g+16, 32g+32); 16 queries = 8 packed columns.
+      auto issue_dkv = [&](int it, int h) {
+        const uint32_t sb = stage(it);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_ss(tmem + TM_R1, sdesc_sw128(vA + off, 16, 1024),
-                 sdesc_sw128(sb + ST_DO + off, 16, 1024), IDESC_ST, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar_addr(sbase, B_SFULL));
-        ok = ctx.wait(B_PFULL, it & 1);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO_i and dK += dS^T Q_i.  R0 holds, for each 32-query
-        // chunk g, P^T packed in columns [32g, 32g+16) and dS^T packed in
-        // [32g+16, 32g+32); a 16-query step is 8 packed columns.  dO_i, Q_i
-        // are MN-major B operands.
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * h + k4;
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           const uint32_t pcol = TM_R0 + 32 * (kk >> 1) + 8 * (kk & 1);
           mma_ts(tmem + TM_DV, tmem + pcol, sdesc_sw128(sb + ST_DO + kk * 2048, HALF, 1024),
@@ -305,27 +301,61 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           mma_ts(tmem + TM_DK, tmem + pcol + 16, sdesc_sw128(sb + ST_Q + kk * 2048, HALF, 1024),
                  IDESC_DKV, acc);
         }
+      };
+      bool ok = ctx.wait(B_KVFULL, 0) && ctx.wait(B_QFULL + 0, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0, false);
+        issue_sdp(0, 0, true);
+        mma_commit(bar_addr(sbase, B_SFULL + 0));
+        issue_sdp(0, 1, false);
+        issue_sdp(0, 1, true);
+        mma_commit(bar_addr(sbase, B_SFULL + 1));
+      }
+      for (int it = 0; it < nit && ok; ++it) {
+        const bool next = it + 1 < nit;
+        if (!(ok = ctx.wait(B_PFULL + 0, it & 1))) break;
+        tc_fence_after();
+        issue_dkv(it, 0);
+        if (!(ok = ctx.wait(B_PFULL + 1, it & 1))) break;
+        tc_fence_after();
         // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1.
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
+        for (int kk = 0; kk < BKV / 16; ++kk)
           mma_ss(tmem + TM_R1, sdesc_sw128(kA + kk * 2048, HALF, 1024),
                  sdesc_sw128(ds + kk * 2048, HALF, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-        }
         mma_commit(bar_addr(sbase, B_DQFULL));
         mma_commit(bar_addr(sbase, B_DSFREE));
-        mma_commit(bar_addr(sbase, B_QEMPTY + st));
+        if (next) {                     // R0's first half was read by dV0/dK0 already
+          if (!(ok = ctx.wait(B_QFULL + ((it + 1) & 1), ((it + 1) >> 1) & 1))) break;
+          tc_fence_after();
+          issue_sdp(it + 1, 0, false);
+        }
+        issue_dkv(it, 1);
+        mma_commit(bar_addr(sbase, B_QEMPTY + (it & 1)));
+        if (next) {                     // R1 is free once the writers drained dQ^T
+          if (!(ok = ctx.wait(B_DQFREE, it & 1))) break;
+          tc_fence_after();
+          issue_sdp(it + 1, 0, true);
+          mma_commit(bar_addr(sbase, B_SFULL + 0));
+          issue_sdp(it + 1, 1, false);
+          issue_sdp(it + 1, 1, true);
+          mma_commit(bar_addr(sbase, B_SFULL + 1));
+        }
       }
       if (ok) mma_commit(bar_addr(sbase, B_DONE));
     }
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    const int half = warp >> 2;                       // query columns [64 half, 64 half + 64)
+    // All eight warps work on each 64-query half in turn: warp w takes the
+    // rows of TMEM lane quadrant w & 3 and the 32-query slice w >> 2 of the
+    // half, so each half's latency is one 32-column chunk per warp.
+    const int sub = warp >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                 // key row within block j
     const int kv = j * BKV + row;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    uint8_t* ds_smem = smem + OFF_DS + half * HALF;
     bool ok = true;
     for (int it = 0; it < nit && ok; ++it) {
       const int st = it & 1;
@@ -334,42 +364,56 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_D);
-      // QFULL: the staged LSE / D are visible here; SFULL: S^T, dP^T in TMEM.
-      if (!ctx.wait(B_QFULL + st, (it >> 1) & 1) || !ctx.wait(B_SFULL, it & 1)) {
+      // QFULL: the staged LSE / D are visible to this thread.
+      if (!ctx.wait(B_QFULL + st, (it >> 1) & 1)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      // Valid queries for this key row: q in [qlo, qhi] (causal: q >= kv;
-      // past the end of the sequence nothing is valid).  Applied as a select,
-      // no branch per element.
+      // Valid queries for this key row: q in [qlo, N - 1] (causal: q >= kv;
+      // past the end of the sequence nothing is valid).  Only the diagonal
+      // block and ragged blocks need it; the test below is the same for the
+      // whole thread block, so the unmasked path has no per-element work.
+      const bool need_mask =
+          (causal && qb == j * BKV) || (qb + BQ > N) || (j * BKV + BKV > N);
       const int qlo = causal ? kv : 0;
-      const int qhi = kv < N ? N - 1 : -1;
+      const uint32_t qspan = kv < N ? static_cast<uint32_t>(N - 1 - qlo) : 0u;
+      const bool row_valid = kv < N;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = half * 64 + c * 32;          // first query column of this chunk
+      for (int h = 0; h < 2; ++h) {
+        if (!ctx.wait(B_SFULL + h, it & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int col0 = h * 64 + sub * 32;           // first query column of this slice
         uint32_t sr[32], dr[32];
         tmem_ld32(tmem + lane_addr + TM_R0 + col0, sr);
         tmem_ld32(tmem + lane_addr + TM_R1 + col0, dr);
         uint32_t pk[16], gk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
+          // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
           const float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
           const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
-          const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], g[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int q = qb + col0 + e + t;
-            p[t] = fast_exp2(fmaf(__uint_as_float(sr[e + t]), scale_log2, -ls[t]));
-            p[t] = (q >= qlo && q <= qhi) ? p[t] : 0.f;
-            g[t] = p[t] * (__uint_as_float(dr[e + t]) - dd[t]);
+          float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
+          float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
+          float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
+          if (need_mask) {
+            // qlo <= q <= N - 1 as one unsigned compare per query (the
+            // wrap-around of rel + t is the exact difference mod 2^32)
+            const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
+            p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
+            p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
+            p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
+            p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
           }
-          pk[e / 2] = pack_bf16x2(p[0], p[1]);
-          pk[e / 2 + 1] = pack_bf16x2(p[2], p[3]);
-          gk[e / 2] = pack_bf16x2(g[0], g[1]);
-          gk[e / 2 + 1] = pack_bf16x2(g[2], g[3]);
+          pk[e / 2] = pack_bf16x2(p0, p1);
+          pk[e / 2 + 1] = pack_bf16x2(p2, p3);
+          gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + d4.x),
+                                  p1 * (__uint_as_float(dr[e + 1]) + d4.y));
+          gk[e / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[e + 2]) + d4.z),
+                                      p3 * (__uint_as_float(dr[e + 3]) + d4.w));
         }
         // Packed P^T and dS^T go over exactly the 32 columns this thread has
         // just read (P^T first 16, dS^T last 16): no other warp reads them.
@@ -377,30 +421,30 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_st16(tmem + lane_addr + TM_R0 + col0 + 16, gk);
         // dS^T row into shared memory (MN-major operand of the dQ product):
         // the previous block's dQ product must have finished reading it.
-        if (c == 0 && it > 0 && !ctx.wait(B_DSFREE, (it - 1) & 1)) {
+        if (h == 0 && it > 0 && !ctx.wait(B_DSFREE, (it - 1) & 1)) {
           ok = false;
           break;
         }
+        uint8_t* ds_smem = smem + OFF_DS + h * HALF;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t off = sw128_offset(row, c * 4 + ch);
+          const uint32_t off = sw128_offset(row, sub * 4 + ch);
           *reinterpret_cast<uint4*>(ds_smem + off) =
               make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
         }
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL + h));
       }
-      if (!ok) break;
-      fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL));
     }
     // dV (warps 0-3) and dK (warps 4-7) leave TMEM once, after every product.
     if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
       tc_fence_after();
-      __nv_bfloat16* out = half == 0 ? dV : dK;
-      const float mul = half == 0 ? 1.f : scale;
-      const uint32_t src = tmem + lane_addr + (half == 0 ? TM_DV : TM_DK);
+      __nv_bfloat16* out = sub == 0 ? dV : dK;
+      const float mul = sub == 0 ? 1.f : scale;
+      const uint32_t src = tmem + lane_addr + (sub == 0 ? TM_DV : TM_DK);
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t r[32];
