@@ -195,8 +195,8 @@ static int backward_impl(const void* q, const void* k, const void* v, const void
   }
   const int BH = B * H;
   fa::BwdMaps maps;
-  if (int r = make_map(&maps.q, q, BH, N, 128)) return r;
-  if (int r = make_map(&maps.dO, dO, BH, N, 128)) return r;
+  if (int r = make_map(&maps.q, q, BH, N, 64)) return r;     // 64-query blocks
+  if (int r = make_map(&maps.dO, dO, BH, N, 64)) return r;
   if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
   if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
   if (own_ws) {

@@ -14,25 +14,26 @@
 //                to a multiple of 128 rows (so every block copy is aligned
 //                and in bounds), and zeroing of the fp32 dQ accumulator.
 //   bwd_main     one thread block per (b, h, 128-key block j).  K_j and V_j
-//                stay in shared memory; 128-row blocks Q_i, dO_i (with their
-//                LSE and D) stream past in a 2-stage TMA ring.  Per block i,
-//                in two 64-query halves that overlap each other's softmax:
-//                  S^T  = K_j Q_i^T   -> TMEM R0      (shared-memory operands)
-//                  dP^T = V_j dO_i^T  -> TMEM R1
+//                stay in shared memory; 64-row blocks Q_i, dO_i (with their
+//                LSE and D) stream past in a 3-stage TMA ring.  Per block i,
+//                in one of two TMEM buffers X = i mod 2:
+//                  S^T  = K_j Q_i^T   -> R0_X   (shared-memory operands)
+//                  dP^T = V_j dO_i^T  -> R1_X
 //                  softmax warps (key row = TMEM lane) form
 //                  P^T = exp2(S^T scale log2e - LSE log2e) and
 //                  dS^T = P^T (dP^T - D), write both as packed bf16 over the
-//                  R0 columns they were computed from, and dS^T also to
-//                  shared memory;
-//                  dV += P^T dO_i, dK += dS^T Q_i   (A operand from TMEM)
-//                  dQ_i^T = K_j^T dS^T -> TMEM R1  (both operands MN-major)
-//                and four writer warps add scale * dQ_i into the fp32
+//                  R0_X columns they were computed from, and dS^T also to
+//                  shared memory (double-buffered);
+//                  dQ_i^T = K_j^T dS^T -> R1_X    (both operands MN-major)
+//                  dV += P^T dO_i, dK += dS^T Q_i  (A operand from TMEM)
+//                Block i's softmax overlaps the products of blocks i-1 and
+//                i+1; four writer warps add scale * dQ_i into the fp32
 //                accumulator with 16-byte vector atomics after a 4x4 register
 //                transpose (one warp instruction covers 4 rows x 128
 //                contiguous bytes).  dK and dV leave TMEM once.
 //   bwd_convert  dQ = bf16(accumulator).
-// Causal: query blocks entirely above the key block are skipped; the
-// diagonal block is masked element-wise.
+// Causal: query blocks entirely above the key block are skipped; the blocks
+// that straddle the diagonal are masked element-wise.
 #include <cfloat>
 
 #include "fa_device.cuh"
@@ -45,33 +46,38 @@ __device__ int g_status_bwd;
 
 constexpr int HD = 128;
 constexpr int BKV = 128;                  // key rows per block (TMEM lanes)
-constexpr int BQ = 128;                   // query rows per streamed block
-constexpr uint32_t TILE = 128 * HD * 2;   // 32 KiB
+constexpr int BQ = 64;                    // query rows per streamed block
+constexpr int PAD = 128;                  // per-head padding of the staged LSE / D
+constexpr int STAGES = 3;
+constexpr uint32_t TILE = 128 * HD * 2;   // K_j or V_j: 32 KiB
 constexpr uint32_t HALF = TILE / 2;       // 128 rows x 64 columns
-constexpr uint32_t STAT = BQ * 4;         // 512 B of LSE*log2e or D per block
+constexpr uint32_t QTILE = BQ * HD * 2;   // Q_i or dO_i: 16 KiB
+constexpr uint32_t QHALF = QTILE / 2;     // 64 rows x 64 columns
+constexpr uint32_t STAT = BQ * 4;         // 256 B of -LSE*log2e or -D per block
+constexpr uint32_t DS_TILE = BKV * BQ * 2;                   // dS^T [key][query]: 16 KiB
 
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + TILE;
-constexpr uint32_t OFF_STAGE = OFF_V + TILE;                 // 2 stages
-constexpr uint32_t ST_Q = 0, ST_DO = TILE, ST_LSE = 2 * TILE, ST_D = 2 * TILE + STAT;
-constexpr uint32_t STAGE_BYTES = 2 * TILE + 2 * STAT;        // 65 KiB (1024-aligned)
-constexpr uint32_t OFF_DS = OFF_STAGE + 2 * STAGE_BYTES;     // dS^T, [key][query] bf16
-constexpr uint32_t OFF_BAR = OFF_DS + TILE;
+constexpr uint32_t OFF_STAGE = OFF_V + TILE;
+constexpr uint32_t ST_Q = 0, ST_DO = QTILE, ST_LSE = 2 * QTILE, ST_D = 2 * QTILE + STAT;
+constexpr uint32_t STAGE_BYTES = 2 * QTILE + 2048;           // 1024-aligned stages
+constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES; // 2 buffers
+constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_TILE;
 constexpr int B_KVFULL = 0;
-constexpr int B_QFULL = 1;     // + stage
-constexpr int B_QEMPTY = 3;    // + stage
-constexpr int B_SFULL = 5;     // + half: S^T and dP^T of 64 queries in TMEM
-constexpr int B_PFULL = 7;     // + half: their P^T, dS^T written (8 softmax warps)
-constexpr int B_DSFREE = 9;    // shared dS^T consumed by the dQ product
-constexpr int B_DQFULL = 10;
-constexpr int B_DQFREE = 11;   // 4 writer warps have read dQ^T
-constexpr int B_DONE = 12;     // every product of the block completed
-constexpr int NBAR = 13;
+constexpr int B_QFULL = 1;                 // + stage
+constexpr int B_QEMPTY = B_QFULL + STAGES; // + stage
+constexpr int B_SFULL = B_QEMPTY + STAGES; // + buffer: S^T and dP^T in TMEM
+constexpr int B_PFULL = B_SFULL + 2;       // + buffer: P^T, dS^T written (8 warps)
+constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
+constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
+constexpr int B_DONE = B_DQFREE + 2;       // every product of the block completed
+constexpr int NBAR = B_DONE + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // base is 1024-aligned (checked)
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_R0 = 0, TM_R1 = 128, TM_DV = 256, TM_DK = 384;
+// buffer X: R0 = [128 X, 128 X + 64), R1 = [128 X + 64, 128 X + 128)
+constexpr uint32_t TM_DV = 256, TM_DK = 384;
 
 constexpr int NTHREADS = 448;   // 0-7 softmax, 8-11 dQ writers, 12 producer, 13 MMA
 constexpr int WARP_TMA = 12;
@@ -79,12 +85,11 @@ constexpr int WARP_MMA = 13;
 constexpr int kHeadGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// S^T = K_j Q_i^T and dP^T = V_j dO_i^T, one 64-query half at a time:
-// M = 128 keys, N = 64 queries.
-constexpr uint32_t IDESC_ST = idesc_bf16(BKV, BQ / 2, false, false);
+// S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 64 queries.
+constexpr uint32_t IDESC_ST = idesc_bf16(BKV, BQ, false, false);
 // dV += P^T dO_i, dK += dS^T Q_i: A in TMEM, B MN-major; M = 128 keys, N = d.
 constexpr uint32_t IDESC_DKV = idesc_bf16(BKV, HD, false, true);
-// dQ_i^T = K_j^T dS^T: M = d, N = 128 queries; both operands MN-major.
+// dQ_i^T = K_j^T dS^T: M = d, N = 64 queries; both operands MN-major.
 constexpr uint32_t IDESC_DQ = idesc_bf16(HD, BQ, true, true);
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
@@ -203,23 +208,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int rem = static_cast<int>(blockIdx.x) - group * per_group;
   const int j = rem / gsize;                          // key block
   const int bh = group * kHeadGroup + rem % gsize;
-  const int i0 = causal ? j : 0;
+  const int i0 = causal ? (j * BKV) / BQ : 0;         // first query block that sees key block j
   const int nit = nqb - i0;
   const float scale_log2 = scale * kLog2e;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(sbase, B_KVFULL), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_addr(sbase, B_QFULL + s), 1);
       mbar_init(bar_addr(sbase, B_QEMPTY + s), 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(bar_addr(sbase, B_SFULL + h), 1);
-      mbar_init(bar_addr(sbase, B_PFULL + h), 8);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar_addr(sbase, B_SFULL + x), 1);
+      mbar_init(bar_addr(sbase, B_PFULL + x), 8);
+      mbar_init(bar_addr(sbase, B_DQFULL + x), 1);
+      mbar_init(bar_addr(sbase, B_DQFREE + x), 4);
     }
-    mbar_init(bar_addr(sbase, B_DSFREE), 1);
-    mbar_init(bar_addr(sbase, B_DQFULL), 1);
-    mbar_init(bar_addr(sbase, B_DQFREE), 4);
     mbar_init(bar_addr(sbase, B_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -247,16 +251,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_load_3d(sbase + OFF_V, &tmV, kvf, 0, j * BKV, bh);
       tma_load_3d(sbase + OFF_V + HALF, &tmV, kvf, 64, j * BKV, bh);
       for (int it = 0; it < nit; ++it) {
-        const int st = it & 1;
+        const int st = it % STAGES;
         const int qb = (i0 + it) * BQ;
-        if (it >= 2 && !ctx.wait(B_QEMPTY + st, ((it >> 1) - 1) & 1)) break;
+        if (it >= STAGES && !ctx.wait(B_QEMPTY + st, ((it / STAGES) - 1) & 1)) break;
         const uint32_t qf = bar_addr(sbase, B_QFULL + st);
         const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
-        mbar_arrive_expect_tx(qf, 2 * TILE + 2 * STAT);
+        mbar_arrive_expect_tx(qf, 2 * QTILE + 2 * STAT);
         tma_load_3d(sb + ST_Q, &tmQ, qf, 0, qb, bh);
-        tma_load_3d(sb + ST_Q + HALF, &tmQ, qf, 64, qb, bh);
+        tma_load_3d(sb + ST_Q + QHALF, &tmQ, qf, 64, qb, bh);
         tma_load_3d(sb + ST_DO, &tmdO, qf, 0, qb, bh);
-        tma_load_3d(sb + ST_DO + HALF, &tmdO, qf, 64, qb, bh);
+        tma_load_3d(sb + ST_DO + QHALF, &tmdO, qf, 64, qb, bh);
         const size_t srow = static_cast<size_t>(bh) * Npad + qb;
         bulk_load(sb + ST_LSE, lse_pad + srow, STAT, qf);
         bulk_load(sb + ST_D, d_pad + srow, STAT, qf);
@@ -265,82 +269,73 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    // Software-pipelined order, per query block i and 64-query half h:
-    //   ... dV0 dK0 | dQ^T(i) S0(i+1) dV1 dK1 | dP0(i+1) S1(i+1) dP1(i+1) | ...
-    // so half 0's softmax overlaps half 1's S/dP products, half 1's softmax
-    // overlaps dV0/dK0, and the writers drain dQ^T(i) while dV1/dK1 run.
+    // Order, per query block i in buffer X = i mod 2:
+    //   [P(i) ready] dQ^T(i) dV(i) dK(i) | S^T(i+2) [dQ^T(i) drained] dP^T(i+2)
+    // so block i+1's softmax overlaps block i's gradient products and block
+    // i+2's score products, and the writers drain dQ^T(i) meanwhile.
     if (lane == 0) {
-      const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V, ds = sbase + OFF_DS;
-      auto stage = [&](int it) { return sbase + OFF_STAGE + (it & 1) * STAGE_BYTES; };
-      // S^T (into R0) or dP^T (into R1) for half h of block `it`: reduction
-      // over d; the half's 64 query rows start 64 * 128 bytes into each
-      // 64-column box of the Q / dO tile.
-      auto issue_sdp = [&](int it, int h, bool dp) {
+      const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V;
+      auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
+      auto r0 = [&](int it) { return tmem + 128u * (it & 1); };
+      auto r1 = [&](int it) { return tmem + 128u * (it & 1) + 64u; };
+      // S^T (into R0) or dP^T (into R1): reduction over d.
+      auto issue_sdp = [&](int it, bool dp) {
         const uint32_t a = dp ? vA : kA;
-        const uint32_t b = stage(it) + (dp ? ST_DO : ST_Q) + h * 64 * 128;
-        const uint32_t d = tmem + (dp ? TM_R1 : TM_R0) + h * 64;
+        const uint32_t b = stage(it) + (dp ? ST_DO : ST_Q);
+        const uint32_t d = dp ? r1(it) : r0(it);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), IDESC_ST,
+          mma_ss(d, sdesc_sw128(a + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(b + (kk >> 2) * QHALF + (kk & 3) * 32, 16, 1024), IDESC_ST,
                  kk > 0 ? 1u : 0u);
         }
       };
-      // dV += P^T dO_i and dK += dS^T Q_i over the 64 queries of half h.  R0
-      // holds, per 32-query chunk g, P^T packed in columns [32g, 32g+16) and
-      // dS^T packed in [32g+16, 32g+32); 16 queries = 8 packed columns.
-      auto issue_dkv = [&](int it, int h) {
-        const uint32_t sb = stage(it);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int kk = 4 * h + k4;
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pcol = TM_R0 + 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tmem + TM_DV, tmem + pcol, sdesc_sw128(sb + ST_DO + kk * 2048, HALF, 1024),
-                 IDESC_DKV, acc);
-          mma_ts(tmem + TM_DK, tmem + pcol + 16, sdesc_sw128(sb + ST_Q + kk * 2048, HALF, 1024),
-                 IDESC_DKV, acc);
-        }
+      auto wait_q = [&](int it) {
+        return ctx.wait(B_QFULL + it % STAGES, (it / STAGES) & 1);
       };
-      bool ok = ctx.wait(B_KVFULL, 0) && ctx.wait(B_QFULL + 0, 0);
-      if (ok) {
+      bool ok = ctx.wait(B_KVFULL, 0);
+      for (int it = 0; it < 2 && it < nit && ok; ++it) {
+        if (!(ok = wait_q(it))) break;
         tc_fence_after();
-        issue_sdp(0, 0, false);
-        issue_sdp(0, 0, true);
-        mma_commit(bar_addr(sbase, B_SFULL + 0));
-        issue_sdp(0, 1, false);
-        issue_sdp(0, 1, true);
-        mma_commit(bar_addr(sbase, B_SFULL + 1));
+        issue_sdp(it, false);
+        issue_sdp(it, true);
+        mma_commit(bar_addr(sbase, B_SFULL + (it & 1)));
       }
       for (int it = 0; it < nit && ok; ++it) {
-        const bool next = it + 1 < nit;
-        if (!(ok = ctx.wait(B_PFULL + 0, it & 1))) break;
+        const int x = it & 1;
+        const uint32_t sb = stage(it);
+        if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
         tc_fence_after();
-        issue_dkv(it, 0);
-        if (!(ok = ctx.wait(B_PFULL + 1, it & 1))) break;
-        tc_fence_after();
-        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1.
+        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
+        const uint32_t ds = sbase + OFF_DS + x * DS_TILE;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_ss(tmem + TM_R1, sdesc_sw128(kA + kk * 2048, HALF, 1024),
-                 sdesc_sw128(ds + kk * 2048, HALF, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-        mma_commit(bar_addr(sbase, B_DQFULL));
-        mma_commit(bar_addr(sbase, B_DSFREE));
-        if (next) {                     // R0's first half was read by dV0/dK0 already
-          if (!(ok = ctx.wait(B_QFULL + ((it + 1) & 1), ((it + 1) >> 1) & 1))) break;
-          tc_fence_after();
-          issue_sdp(it + 1, 0, false);
+          mma_ss(r1(it), sdesc_sw128(kA + kk * 2048, HALF, 1024),
+                 sdesc_sw128(ds + kk * 2048, DS_TILE, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
+        mma_commit(bar_addr(sbase, B_DQFULL + x));
+        // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
+        // P^T packed in columns [32g, 32g+16) and dS^T in [32g+16, 32g+32);
+        // 16 queries = 8 packed columns.
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t pcol = r0(it) + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_ts(tmem + TM_DV, pcol, sdesc_sw128(sb + ST_DO + kk * 2048, QHALF, 1024),
+                 IDESC_DKV, acc);
+          mma_ts(tmem + TM_DK, pcol + 16, sdesc_sw128(sb + ST_Q + kk * 2048, QHALF, 1024),
+                 IDESC_DKV, acc);
         }
-        issue_dkv(it, 1);
-        mma_commit(bar_addr(sbase, B_QEMPTY + (it & 1)));
-        if (next) {                     // R1 is free once the writers drained dQ^T
-          if (!(ok = ctx.wait(B_DQFREE, it & 1))) break;
+        mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
+        if (it + 2 < nit) {
+          // R0_X was read by dV/dK(i) (issued above, executed in order).
+          if (!(ok = wait_q(it + 2))) break;
           tc_fence_after();
-          issue_sdp(it + 1, 0, true);
-          mma_commit(bar_addr(sbase, B_SFULL + 0));
-          issue_sdp(it + 1, 1, false);
-          issue_sdp(it + 1, 1, true);
-          mma_commit(bar_addr(sbase, B_SFULL + 1));
+          issue_sdp(it + 2, false);
+          // R1_X holds dQ^T(i) until the writers have read it.
+          if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
+          tc_fence_after();
+          issue_sdp(it + 2, true);
+          mma_commit(bar_addr(sbase, B_SFULL + x));
         }
       }
       if (ok) mma_commit(bar_addr(sbase, B_DONE));
@@ -348,96 +343,87 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    // All eight warps work on each 64-query half in turn: warp w takes the
-    // rows of TMEM lane quadrant w & 3 and the 32-query slice w >> 2 of the
-    // half, so each half's latency is one 32-column chunk per warp.
+    // Warp w takes the rows of TMEM lane quadrant w & 3 and the 32-query
+    // slice w >> 2 of each 64-query block.
     const int sub = warp >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                 // key row within block j
     const int kv = j * BKV + row;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const int qlo = causal ? kv : 0;
+    const uint32_t qspan = kv < N ? static_cast<uint32_t>(N - 1 - qlo) : 0u;
+    const bool row_valid = kv < N;
     bool ok = true;
-    for (int it = 0; it < nit && ok; ++it) {
-      const int st = it & 1;
+    for (int it = 0; it < nit; ++it) {
+      const int x = it & 1;
+      const int st = it % STAGES;
       const int qb = (i0 + it) * BQ;
       const float* stage_lse =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_D);
-      // QFULL: the staged LSE / D are visible to this thread.
-      if (!ctx.wait(B_QFULL + st, (it >> 1) & 1)) {
+      // QFULL: the staged LSE / D are visible here; SFULL: S^T, dP^T in TMEM.
+      // SFULL(i) is committed after dQ^T(i-2), the last reader of this
+      // block's dS^T shared buffer, so the buffer is free as well.
+      if (!ctx.wait(B_QFULL + st, (it / STAGES) & 1) ||
+          !ctx.wait(B_SFULL + x, (it >> 1) & 1)) {
         ok = false;
         break;
       }
+      tc_fence_after();
       // Valid queries for this key row: q in [qlo, N - 1] (causal: q >= kv;
-      // past the end of the sequence nothing is valid).  Only the diagonal
-      // block and ragged blocks need it; the test below is the same for the
-      // whole thread block, so the unmasked path has no per-element work.
+      // past the end of the sequence nothing is valid).  Only blocks on the
+      // diagonal or at a ragged end need it; the test is block-uniform.
       const bool need_mask =
-          (causal && qb == j * BKV) || (qb + BQ > N) || (j * BKV + BKV > N);
-      const int qlo = causal ? kv : 0;
-      const uint32_t qspan = kv < N ? static_cast<uint32_t>(N - 1 - qlo) : 0u;
-      const bool row_valid = kv < N;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (!ctx.wait(B_SFULL + h, it & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int col0 = h * 64 + sub * 32;           // first query column of this slice
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_addr + TM_R0 + col0, sr);
-        tmem_ld32(tmem + lane_addr + TM_R1 + col0, dr);
-        uint32_t pk[16], gk[16];
+          (causal && qb < j * BKV + BKV) || (qb + BQ > N) || (j * BKV + BKV > N);
+      const int col0 = sub * 32;                      // first query column of this slice
+      const uint32_t s_addr = tmem + lane_addr + 128u * x + col0;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(s_addr, sr);
+      tmem_ld32(s_addr + 64, dr);
+      uint32_t pk[16], gk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
-          const float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
-          float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
-          float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
-          float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
-          if (need_mask) {
-            // qlo <= q <= N - 1 as one unsigned compare per query (the
-            // wrap-around of rel + t is the exact difference mod 2^32)
-            const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
-            p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
-            p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
-            p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
-            p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
-          }
-          pk[e / 2] = pack_bf16x2(p0, p1);
-          pk[e / 2 + 1] = pack_bf16x2(p2, p3);
-          gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + d4.x),
-                                  p1 * (__uint_as_float(dr[e + 1]) + d4.y));
-          gk[e / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[e + 2]) + d4.z),
-                                      p3 * (__uint_as_float(dr[e + 3]) + d4.w));
+      for (int e = 0; e < 32; e += 4) {
+        // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
+        const float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
+        const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
+        float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
+        float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
+        float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
+        float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
+        if (need_mask) {
+          // qlo <= q <= N - 1 as one unsigned compare per query (the
+          // wrap-around of rel + t is the exact difference mod 2^32)
+          const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
+          p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
+          p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
+          p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
+          p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
         }
-        // Packed P^T and dS^T go over exactly the 32 columns this thread has
-        // just read (P^T first 16, dS^T last 16): no other warp reads them.
-        tmem_st16(tmem + lane_addr + TM_R0 + col0, pk);
-        tmem_st16(tmem + lane_addr + TM_R0 + col0 + 16, gk);
-        // dS^T row into shared memory (MN-major operand of the dQ product):
-        // the previous block's dQ product must have finished reading it.
-        if (h == 0 && it > 0 && !ctx.wait(B_DSFREE, (it - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        uint8_t* ds_smem = smem + OFF_DS + h * HALF;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t off = sw128_offset(row, sub * 4 + ch);
-          *reinterpret_cast<uint4*>(ds_smem + off) =
-              make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
-        }
-        fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL + h));
+        pk[e / 2] = pack_bf16x2(p0, p1);
+        pk[e / 2 + 1] = pack_bf16x2(p2, p3);
+        gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + d4.x),
+                                p1 * (__uint_as_float(dr[e + 1]) + d4.y));
+        gk[e / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[e + 2]) + d4.z),
+                                    p3 * (__uint_as_float(dr[e + 3]) + d4.w));
       }
+      // Packed P^T and dS^T go over exactly the 32 columns this thread has
+      // just read (P^T first 16, dS^T last 16): no other warp reads them.
+      tmem_st16(s_addr, pk);
+      tmem_st16(s_addr + 16, gk);
+      // dS^T row into this block's shared buffer (MN-major operand of dQ^T).
+      uint8_t* ds_smem = smem + OFF_DS + x * DS_TILE;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t off = sw128_offset(row, sub * 4 + ch);
+        *reinterpret_cast<uint4*>(ds_smem + off) =
+            make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL + x));
     }
     // dV (warps 0-3) and dK (warps 4-7) leave TMEM once, after every product.
     if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
@@ -467,20 +453,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int quad = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
     for (int it = 0; it < nit; ++it) {
+      const int x = it & 1;
       const int qb = (i0 + it) * BQ;
-      if (!ctx.wait(B_DQFULL, it & 1)) break;
+      if (!ctx.wait(B_DQFULL + x, (it >> 1) & 1)) break;
       tc_fence_after();
       float g[BQ];
 #pragma unroll
       for (int c = 0; c < BQ / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + TM_R1 + c * 32, r);
+        tmem_ld32(tmem + lane_addr + 128u * x + 64 + c * 32, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) g[c * 32 + i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE));
+      if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE + x));
       // Per group of 4 queries, transpose within each 4-lane group so that a
       // lane holds 4 consecutive head-dimension values of one query row:
       // one warp instruction then adds 4 rows x 128 contiguous bytes.
@@ -489,10 +476,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     quad * 32 + (lane & ~3);
 #pragma unroll
       for (int q0 = 0; q0 < BQ; q0 += 4) {
-        float x[4] = {g[q0] * scale, g[q0 + 1] * scale, g[q0 + 2] * scale, g[q0 + 3] * scale};
-        transpose4(x, lane);
+        float v[4] = {g[q0] * scale, g[q0 + 1] * scale, g[q0 + 2] * scale, g[q0 + 3] * scale};
+        transpose4(v, lane);
         if (q0 + (lane & 3) < lim)
-          red_add_v4(base + static_cast<size_t>(q0) * HD, x[0], x[1], x[2], x[3]);
+          red_add_v4(base + static_cast<size_t>(q0) * HD, v[0], v[1], v[2], v[3]);
       }
     }
   }
@@ -505,7 +492,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
-size_t padded_len(int N) { return (static_cast<size_t>(N) + BQ - 1) / BQ * BQ; }
+size_t padded_len(int N) { return (static_cast<size_t>(N) + PAD - 1) / PAD * PAD; }
 
 }  // namespace
 

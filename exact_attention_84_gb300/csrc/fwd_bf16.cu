@@ -98,26 +98,34 @@ struct Ctx {
   }
 };
 
+// S = Q K^T for Q block `blk` against the K tile in `kslot`: 8 k-steps of
+// 16 along d, both operands K-major (128-byte rows, two 64-column boxes).
 __device__ __forceinline__ void issue_s(const Ctx& c, uint32_t tmem, int blk, uint32_t kslot) {
-  const uint32_t q = c.sbase + (blk ? OFF_QB : OFF_QA);
-  const uint32_t k = c.sbase + OFF_SLOT + kslot * TILE_BYTES;
+  const uint64_t qd = sdesc_sw128(c.sbase + (blk ? OFF_QB : OFF_QA), 16, 1024);
+  const uint64_t kd = sdesc_sw128(c.sbase + OFF_SLOT + kslot * TILE_BYTES, 16, 1024);
+  uint64_t a[8], b[8];
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-    mma_ss(tmem + TM_S + 128 * blk, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024),
-           IDESC_S, kk > 0 ? 1u : 0u);
+    const uint64_t off = ((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4;   // descriptor units
+    a[kk] = qd + off;
+    b[kk] = kd + off;
   }
+  mma_ss_batch8(tmem + TM_S + 128 * blk, a, b, IDESC_S, 0u);
 }
 
+// O (+)= P V for Q block `blk`: P packed in TMEM (16 keys = 8 columns per
+// step), V tile MN-major (16 key rows = 2048 bytes per step).
 __device__ __forceinline__ void issue_pv(const Ctx& c, uint32_t tmem, int blk, uint32_t vslot,
                                          bool first) {
-  const uint32_t v = c.sbase + OFF_SLOT + vslot * TILE_BYTES;
+  const uint64_t vd = sdesc_sw128(c.sbase + OFF_SLOT + vslot * TILE_BYTES, HALF_BYTES, 1024);
+  uint32_t a[8];
+  uint64_t b[8];
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
-    // P: 16 keys = 8 packed columns per step; V: 16 key rows = 2048 bytes.
-    mma_ts(tmem + TM_O + 128 * blk, tmem + TM_S + 128 * blk + kk * 8,
-           sdesc_sw128(v + kk * 2048, HALF_BYTES, 1024), IDESC_O, (!first || kk > 0) ? 1u : 0u);
+    a[kk] = tmem + TM_S + 128 * blk + kk * 8;
+    b[kk] = vd + ((kk * 2048) >> 4);
   }
+  mma_ts_batch8(tmem + TM_O + 128 * blk, a, b, IDESC_O, first ? 0u : 1u);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
