@@ -278,17 +278,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
       auto r0 = [&](int it) { return tmem + 128u * (it & 1); };
       auto r1 = [&](int it) { return tmem + 128u * (it & 1) + 64u; };
+      // Descriptors of the key-block operands, fixed for the whole block; a
+      // k-step advances the start-address field (units of 16 bytes).
+      const uint64_t kd_k = sdesc_sw128(kA, 16, 1024);        // K_j, K-major (S^T)
+      const uint64_t vd_k = sdesc_sw128(vA, 16, 1024);        // V_j, K-major (dP^T)
+      const uint64_t kd_mn = sdesc_sw128(kA, HALF, 1024);     // K_j^T, MN-major (dQ^T)
       // S^T (into R0) or dP^T (into R1): reduction over d.
       auto issue_sdp = [&](int it, bool dp) {
-        const uint32_t a = dp ? vA : kA;
-        const uint32_t b = stage(it) + (dp ? ST_DO : ST_Q);
-        const uint32_t d = dp ? r1(it) : r0(it);
+        const uint64_t ad = dp ? vd_k : kd_k;
+        const uint64_t bd = sdesc_sw128(stage(it) + (dp ? ST_DO : ST_Q), 16, 1024);
+        uint64_t a[8], b[8];
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_ss(d, sdesc_sw128(a + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(b + (kk >> 2) * QHALF + (kk & 3) * 32, 16, 1024), IDESC_ST,
-                 kk > 0 ? 1u : 0u);
+          a[kk] = ad + (((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+          b[kk] = bd + (((kk >> 2) * QHALF + (kk & 3) * 32) >> 4);
         }
+        mma_ss_batch8(dp ? r1(it) : r0(it), a, b, IDESC_ST, 0u);
       };
       auto wait_q = [&](int it) {
         return ctx.wait(B_QFULL + it % STAGES, (it / STAGES) & 1);
@@ -307,23 +312,35 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
         tc_fence_after();
         // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
-        const uint32_t ds = sbase + OFF_DS + x * DS_TILE;
+        {
+          const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
+          uint64_t a[8], b[8];
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_ss(r1(it), sdesc_sw128(kA + kk * 2048, HALF, 1024),
-                 sdesc_sw128(ds + kk * 2048, DS_TILE, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            a[kk] = kd_mn + ((kk * 2048) >> 4);
+            b[kk] = dsd + ((kk * 2048) >> 4);
+          }
+          mma_ss_batch8(r1(it), a, b, IDESC_DQ, 0u);
+        }
         mma_commit(bar_addr(sbase, B_DQFULL + x));
         // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
         // P^T packed in columns [32g, 32g+16) and dS^T in [32g+16, 32g+32);
         // 16 queries = 8 packed columns.
+        {
+          const uint64_t dod = sdesc_sw128(sb + ST_DO, QHALF, 1024);   // dO_i, MN-major
+          const uint64_t qd = sdesc_sw128(sb + ST_Q, QHALF, 1024);     // Q_i, MN-major
+          uint32_t ap[4], as[4];
+          uint64_t bo[4], bq[4];
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pcol = r0(it) + 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tmem + TM_DV, pcol, sdesc_sw128(sb + ST_DO + kk * 2048, QHALF, 1024),
-                 IDESC_DKV, acc);
-          mma_ts(tmem + TM_DK, pcol + 16, sdesc_sw128(sb + ST_Q + kk * 2048, QHALF, 1024),
-                 IDESC_DKV, acc);
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            ap[kk] = r0(it) + 32 * (kk >> 1) + 8 * (kk & 1);
+            as[kk] = ap[kk] + 16;
+            bo[kk] = dod + ((kk * 2048) >> 4);
+            bq[kk] = qd + ((kk * 2048) >> 4);
+          }
+          const uint32_t acc = it > 0 ? 1u : 0u;
+          mma_ts_batch4(tmem + TM_DV, ap, bo, IDESC_DKV, acc);
+          mma_ts_batch4(tmem + TM_DK, as, bq, IDESC_DKV, acc);
         }
         mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
         if (it + 2 < nit) {
