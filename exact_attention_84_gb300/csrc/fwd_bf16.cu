@@ -284,12 +284,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       tc_fence_after();
       float s[BN];
+      {
+        uint32_t r[BN];
+        tmem_ld128(s_addr, r);                    // the row's 128 scores in one round trip
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
       }
       // mask: causal diagonal tile, or keys past the end of the sequence
       const bool diag = causal && (j == qt);
