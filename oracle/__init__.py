@@ -5,6 +5,9 @@ import this package; the CUDA library never does.
 """
 
 from .attention import (  # noqa: F401
+    attention_backward_gqa,
+    attention_decode_gqa,
+    attention_forward_gqa,
     attention_backward,
     attention_decode,
     attention_forward,

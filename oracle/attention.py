@@ -49,6 +49,9 @@ import math
 import numpy as np
 
 __all__ = [
+    "attention_forward_gqa",
+    "attention_backward_gqa",
+    "attention_decode_gqa",
     "attention_forward",
     "attention_forward_rows",
     "attention_backward",
@@ -62,7 +65,7 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def _head_forward(q, k, v, scale, causal, rows):
+def _head_forward(q, k, v, scale, causal, rows, window=None):
     """One head: q [Nq, d] (the query rows listed in ``rows``), k/v [Nk, d].
 
     Step 1 of "Le probleme": S = Q.K^T (times scale, "FlashAttention
@@ -74,6 +77,10 @@ def _head_forward(q, k, v, scale, causal, rows):
     if causal:
         cols = np.arange(k.shape[0])[None, :]
         s = np.where(cols > np.asarray(rows)[:, None], -np.inf, s)
+    if window is not None:
+        # sliding window: query i sees keys i - window + 1 .. i
+        cols = np.arange(k.shape[0])[None, :]
+        s = np.where(cols < np.asarray(rows)[:, None] - window + 1, -np.inf, s)
     m = s.max(axis=1)                          # row maximum
     e = np.exp(s - m[:, None])                 # exp(-inf) = 0 for masked keys
     l = e.sum(axis=1)                          # row sum of exponentials
@@ -100,16 +107,17 @@ def attention_forward(q, k, v, scale: float, causal: bool):
     return o, lse
 
 
-def attention_forward_rows(q_rows, k, v, rows, scale: float, causal: bool):
+def attention_forward_rows(q_rows, k, v, rows, scale: float, causal: bool, window=None):
     """The same definition for a chosen subset of query rows of ONE head.
 
     ``q_rows`` [R, d] are the query vectors at positions ``rows`` (needed for
     the causal mask); ``k``, ``v`` [N, d] are the head's full key/value
     matrices.  Each output row depends only on its own query row, so this is
-    the definition evaluated row by row, not a blocking of it.
+    the definition evaluated row by row, not a blocking of it.  ``window``
+    (optional) applies the sliding-window mask described further down.
     """
     o, lse, _ = _head_forward(_f64(q_rows), _f64(k), _f64(v), scale, causal,
-                              np.asarray(rows))
+                              np.asarray(rows), window)
     return o, lse
 
 
@@ -203,3 +211,76 @@ def tiled_attention_row(q, k, v, scale: float, tile: int):
         o = corr * o + p @ v[start:start + tile]
         m = m_new
     return o / l, m + math.log(l)
+
+
+# --------------------------------------------------------------------------
+# Grouped query heads and a causal sliding window.
+#
+# Grouped-query attention ("FlashAttention ontleed", "Interactie met de
+# KV-cache": several query heads share the same key and value heads): with
+# Hq query heads and Hkv key/value heads, query head h reads key/value head
+# h // (Hq / Hkv).  Sliding window ("03. FlashAttention", "Variantes et
+# extensions": only the K_j inside the window are considered): query i sees
+# keys i - window + 1 .. i (used together with the causal mask).
+# --------------------------------------------------------------------------
+def _kv_head(h, hq, hkv):
+    return h // (hq // hkv)
+
+
+def attention_forward_gqa(q, k, v, scale: float, causal: bool, window=None):
+    """q [B, Hq, N, d], k/v [B, Hkv, N, d] -> (O [B, Hq, N, d], LSE [B, Hq, N])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, hq, n, _ = q.shape
+    hkv = k.shape[1]
+    o = np.empty(q.shape[:-1] + (v.shape[-1],), dtype=np.float64)
+    lse = np.empty(q.shape[:-1], dtype=np.float64)
+    rows = np.arange(n)
+    for b in range(B):
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            o[b, h], lse[b, h], _ = _head_forward(q[b, h], k[b, g], v[b, g], scale, causal, rows,
+                                                  window)
+    return o, lse
+
+
+def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None):
+    """Gradients for grouped heads: dQ per query head; dK, dV of a key/value
+    head are the sums over the query heads that read it."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, hq, n, _ = q.shape
+    hkv = k.shape[1]
+    rows = np.arange(n)
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            o, _, p = _head_forward(q[b, h], k[b, g], v[b, g], scale, causal, rows, window)
+            gr = do[b, h]
+            dv[b, g] += p.T @ gr                  # dV summed over the group
+            dpg = gr @ v[b, g].T
+            dsum = (gr * o).sum(axis=1)           # D_i = dO_i . O_i
+            dsg = p * (dpg - dsum[:, None])
+            dq[b, h] = scale * (dsg @ k[b, g])
+            dk[b, g] += scale * (dsg.T @ q[b, h])  # dK summed over the group
+    return dq, dk, dv
+
+
+def attention_decode_gqa(q, kcache, vcache, scale: float):
+    """q [B, Hq, d], caches [B, Hkv, L, d] -> (o [B, Hq, d], lse [B, Hq])."""
+    q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+    B, hq, _ = q.shape
+    hkv = kc.shape[1]
+    o = np.empty(q.shape[:-1] + (vc.shape[-1],), dtype=np.float64)
+    lse = np.empty((B, hq), dtype=np.float64)
+    for b in range(B):
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            s = (kc[b, g] @ q[b, h]) * scale
+            m = s.max()
+            e = np.exp(s - m)
+            l = e.sum()
+            o[b, h] = (e @ vc[b, g]) / l
+            lse[b, h] = m + math.log(l)
+    return o, lse

@@ -314,6 +314,119 @@ def pin_rows_subset(orc):
     assert np.abs(oc - on).max() < 1e-14 and np.abs(lc - ln).max() < 1e-14
 
 
+def brute_forward_window(q, k, v, scale, window):
+    """Scalar loop: causal attention of row i over keys max(0, i-window+1)..i."""
+    n = len(q)
+    o = np.zeros((n, len(v[0])))
+    lse = np.zeros(n)
+    for i in range(n):
+        js = range(max(0, i - window + 1), i + 1)
+        sc = {j: scale * math.fsum(q[i][t] * k[j][t] for t in range(len(q[0]))) for j in js}
+        top = max(sc.values())
+        w = {j: math.exp(x - top) for j, x in sc.items()}
+        tot = math.fsum(w.values())
+        for c in range(len(v[0])):
+            o[i, c] = math.fsum(w[j] * v[j][c] for j in js) / tot
+        lse[i] = top + math.log(tot)
+    return o, lse
+
+
+def pin_gqa_repeat_kv(orc):
+    """Grouped heads are ordinary heads over repeated K/V: query head h reads
+    key/value head h // (Hq/Hkv), so the grouped result equals the pinned
+    per-head definition on K/V repeated group-wise, and the grouped dK, dV are
+    the per-head gradients summed over each group."""
+    r = _rng(51)
+    b, hq, hkv, n, d = 2, 6, 2, 9, 4
+    q, do = (r.standard_normal((b, hq, n, d)) for _ in range(2))
+    k, v = (r.standard_normal((b, hkv, n, d)) for _ in range(2))
+    grp = hq // hkv
+    kr, vr = np.repeat(k, grp, axis=1), np.repeat(v, grp, axis=1)
+    for causal in (False, True):
+        o, lse = orc.attention_forward_gqa(q, k, v, 0.5, causal)
+        om, lm = orc.attention_forward(q, kr, vr, 0.5, causal)
+        assert np.abs(o - om).max() < 1e-14 and np.abs(lse - lm).max() < 1e-14
+        dq, dk, dv = orc.attention_backward_gqa(q, k, v, do, 0.5, causal)
+        dqm, dkm, dvm = orc.attention_backward(q, kr, vr, do, 0.5, causal)
+        assert np.abs(dq - dqm).max() < 1e-13
+        assert np.abs(dk - dkm.reshape(b, hkv, grp, n, d).sum(axis=2)).max() < 1e-13
+        assert np.abs(dv - dvm.reshape(b, hkv, grp, n, d).sum(axis=2)).max() < 1e-13
+    # one group (Hkv = Hq) is the per-head definition itself
+    o1, l1 = orc.attention_forward_gqa(q, q, do, 0.5, True)
+    om1, lm1 = orc.attention_forward(q, q, do, 0.5, True)
+    assert np.abs(o1 - om1).max() < 1e-15 and np.abs(l1 - lm1).max() < 1e-15
+    qd = r.standard_normal((b, hq, d))
+    kc, vc = (r.standard_normal((b, hkv, 13, d)) for _ in range(2))
+    od, ld = orc.attention_decode_gqa(qd, kc, vc, 0.5)
+    odm, ldm = orc.attention_decode(qd, np.repeat(kc, grp, axis=1), np.repeat(vc, grp, axis=1),
+                                    0.5)
+    assert np.abs(od - odm).max() < 1e-14 and np.abs(ld - ldm).max() < 1e-14
+
+
+def pin_window_closed_forms(orc):
+    """Sliding window: width 1 leaves one key per row (O_i = V_i, LSE_i =
+    scale q_i.k_i); width >= N is plain causal attention; otherwise a scalar
+    loop over the window's keys."""
+    r = _rng(53)
+    n, d = 11, 3
+    q, k, v, do = (r.standard_normal((1, 1, n, d)) for _ in range(4))
+    o, lse = orc.attention_forward_gqa(q, k, v, 0.7, True, window=1)
+    assert np.abs(o - v).max() < 1e-15
+    assert np.abs(lse[0, 0] - 0.7 * (q[0, 0] * k[0, 0]).sum(axis=1)).max() < 1e-14
+    dq, dk, dv = orc.attention_backward_gqa(q, k, v, do, 0.7, True, window=1)
+    assert np.abs(dv - do).max() < 1e-15       # P = I
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    for w in (n, n + 5):
+        ow, lw = orc.attention_forward_gqa(q, k, v, 0.7, True, window=w)
+        oc, lc = orc.attention_forward(q, k, v, 0.7, True)
+        assert np.abs(ow - oc).max() < 1e-15 and np.abs(lw - lc).max() < 1e-15
+    for w in (2, 4, 7):
+        ob, lb = brute_forward_window(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(),
+                                      0.7, w)
+        ow, lw = orc.attention_forward_gqa(q, k, v, 0.7, True, window=w)
+        assert np.abs(ow[0, 0] - ob).max() < 1e-13 and np.abs(lw[0, 0] - lb).max() < 1e-13
+        rows = np.array([0, w - 1, w, n - 1])
+        orow, lrow = orc.attention_forward_rows(q[0, 0, rows], k[0, 0], v[0, 0], rows, 0.7,
+                                                True, window=w)
+        assert np.abs(orow - ob[rows]).max() < 1e-13 and np.abs(lrow - lb[rows]).max() < 1e-13
+
+
+def pin_gqa_window_torch(orc):
+    """Library special case: PyTorch's fp64 attention with grouped heads and
+    an explicit boolean window mask, and its autograd gradients."""
+    import torch
+    import torch.nn.functional as F
+
+    g = torch.Generator().manual_seed(7)
+    b, hq, hkv, n, d = 2, 4, 2, 37, 8
+    q, do = (torch.randn(b, hq, n, d, generator=g, dtype=torch.float64) for _ in range(2))
+    k, v = (torch.randn(b, hkv, n, d, generator=g, dtype=torch.float64) for _ in range(2))
+    idx = torch.arange(n)
+    for window in (None, 5, 16):
+        allowed = idx[None, :] <= idx[:, None]
+        if window is not None:
+            allowed &= idx[None, :] > idx[:, None] - window
+        qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+        ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=allowed, scale=0.3,
+                                             enable_gqa=True)
+        ref.backward(do)
+        o, lse = orc.attention_forward_gqa(q.numpy(), k.numpy(), v.numpy(), 0.3, True, window)
+        assert np.abs(o - ref.detach().numpy()).max() < 1e-12
+        s = (q @ k.repeat_interleave(hq // hkv, dim=1).transpose(-1, -2)) * 0.3
+        s = s.masked_fill(~allowed, float("-inf"))
+        assert np.abs(lse - torch.logsumexp(s, dim=-1).numpy()).max() < 1e-12
+        dq, dk, dv = orc.attention_backward_gqa(q.numpy(), k.numpy(), v.numpy(), do.numpy(),
+                                                0.3, True, window)
+        assert np.abs(dq - qq.grad.numpy()).max() < 1e-12
+        assert np.abs(dk - kk.grad.numpy()).max() < 1e-12
+        assert np.abs(dv - vv.grad.numpy()).max() < 1e-12
+    q1 = torch.randn(3, 8, 1, 16, generator=g, dtype=torch.float64)
+    kc, vc = (torch.randn(3, 2, 40, 16, generator=g, dtype=torch.float64) for _ in range(2))
+    ref = F.scaled_dot_product_attention(q1, kc, vc, scale=0.25, enable_gqa=True)
+    od, _ = orc.attention_decode_gqa(q1[:, :, 0].numpy(), kc.numpy(), vc.numpy(), 0.25)
+    assert np.abs(od - ref[:, :, 0].numpy()).max() < 1e-12
+
+
 ALL_PINS = [
     pin_walkthrough_softmax,
     pin_walkthrough_online,
@@ -326,4 +439,7 @@ ALL_PINS = [
     pin_backward_identities,
     pin_torch_sdpa,
     pin_rows_subset,
+    pin_gqa_repeat_kv,
+    pin_window_closed_forms,
+    pin_gqa_window_torch,
 ]

@@ -30,6 +30,16 @@ MUTANTS = {
     "decode_lse_no_max": ("lse[idx] = m + math.log(l)", "lse[idx] = math.log(l)"),
     "online_no_rescale": ("l = l * math.exp(m - m_new) + float(np.exp(c - m_new).sum())",
                           "l = l + float(np.exp(c - m_new).sum())"),
+    "gqa_head_modulo": ("return h // (hq // hkv)", "return h % hkv"),
+    "gqa_dk_overwritten": ("dk[b, g] += scale * (dsg.T @ q[b, h])",
+                           "dk[b, g] = scale * (dsg.T @ q[b, h])"),
+    "gqa_dv_overwritten": ("dv[b, g] += p.T @ gr", "dv[b, g] = p.T @ gr"),
+    "gqa_dk_wrong_operand": ("dk[b, g] += scale * (dsg.T @ q[b, h])",
+                             "dk[b, g] += scale * (dsg.T @ k[b, g])"),
+    "gqa_decode_head": ("s = (kc[b, g] @ q[b, h]) * scale", "s = (kc[b, h % hkv] @ q[b, h]) * scale"),
+    "window_one_too_wide": ("np.asarray(rows)[:, None] - window + 1", "np.asarray(rows)[:, None] - window"),
+    "window_one_too_narrow": ("np.asarray(rows)[:, None] - window + 1",
+                              "np.asarray(rows)[:, None] - window + 2"),
     "tiled_no_out_rescale": ("o = corr * o + p @ v[start:start + tile]",
                              "o = o + p @ v[start:start + tile]"),
 }
