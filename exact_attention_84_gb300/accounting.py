@@ -22,6 +22,21 @@ def backward_flops(B, H, N, d, causal):
     return 2.5 * forward_flops(B, H, N, d, causal)
 
 
+def visible_pairs(N, causal, window=0):
+    """Number of (query, key) pairs the mask leaves visible in one head: the
+    exact count N^2, N(N+1)/2 (causal), or sum_i min(i+1, w) (window w)."""
+    if window and causal and window < N:
+        return window * (window + 1) // 2 + (N - window) * window
+    return N * (N + 1) // 2 if causal else N * N
+
+
+def masked_forward_flops(B, H, N, d, causal, window=0):
+    """4 d FLOPs per visible (query, key) pair and query head.  Only the
+    windowed workloads use it: the plain forward keeps the N^2 / 2 causal
+    convention above."""
+    return 4.0 * B * H * d * visible_pairs(N, causal, window)
+
+
 def forward_min_bytes(B, H, N, d, elem=2):
     """Q, K, V read once, O written once, fp32 LSE written once."""
     return 4 * B * H * N * d * elem + 4 * B * H * N
@@ -33,7 +48,8 @@ def backward_min_bytes(B, H, N, d, elem=2):
 
 
 def decode_kv_bytes(B, H, L, d, elem=2):
-    """The KV cache read once: the algorithmic traffic of one decode call."""
+    """The KV cache read once: the algorithmic traffic of one decode call
+    (H = key/value heads: with grouped query heads the cache has Hkv)."""
     return 2 * B * H * L * d * elem
 
 

@@ -24,9 +24,15 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
-    """O, LSE = attention(q, k, v) for [B, H, N, d] bf16 (or fp32) tensors."""
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            window: int = 0):
+    """O, LSE = attention(q, k, v) for [B, H, N, d] bf16 (or fp32) tensors.
+
+    bf16 only: k and v may have fewer heads Hkv (H a multiple of Hkv; query
+    head h reads key/value head h // (H // Hkv)), and ``window`` w >= 1 (with
+    ``causal``) lets query i see keys i-w+1 .. i only."""
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     fp32 = q.dtype == torch.float32
     dtype = torch.float32 if fp32 else torch.bfloat16
@@ -34,17 +40,26 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         _need(t, dtype, n)
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
-    fn = _lib.fa_forward_fp32 if fp32 else _lib.fa_forward
-    _lib.check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                  B, H, N, d, scale, int(causal), _stream()))
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+    if Hkv != H or window:
+        if fp32:
+            raise ValueError("grouped heads and windows need bf16 tensors")
+        _lib.check(_lib.fa_forward_gqa(*ptrs, B, H, Hkv, N, d, scale, int(causal), int(window),
+                                       _stream()))
+    else:
+        fn = _lib.fa_forward_fp32 if fp32 else _lib.fa_forward
+        _lib.check(fn(*ptrs, B, H, N, d, scale, int(causal), _stream()))
     return o, lse
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-             workspace=None, out=None):
+             workspace=None, out=None, window: int = 0):
     """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``.
-    ``out`` may hold three preallocated tensors (dq, dk, dv) to write into."""
+    ``out`` may hold three preallocated tensors (dq, dk, dv) to write into.
+    k, v (and dk, dv) may have fewer heads, and ``window`` applies, as in
+    ``forward``."""
     B, H, N, d = q.shape
+    Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _need(t, torch.bfloat16, n)
@@ -55,10 +70,15 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
         dq, dk, dv = out
         for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
             _need(t, torch.bfloat16, n)
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale,
-            int(causal))
-    if workspace is None:
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    args = ptrs + (B, H, N, d, scale, int(causal))
+    if Hkv != H or window:
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _lib.check(_lib.fa_backward_gqa(*ptrs, B, H, Hkv, N, d, scale, int(causal), int(window),
+                                        ws_ptr, ws_bytes, _stream()))
+    elif workspace is None:
         _lib.check(_lib.fa_backward(*args, _stream()))
     else:
         _lib.check(_lib.fa_backward_ex(*args, workspace.data_ptr(), workspace.numel() *
@@ -69,13 +89,23 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
 def decode(q, kcache, vcache, num_splits: int = 1, scale: float | None = None,
            with_lse: bool = False, workspace=None):
     """o (and optionally lse) for one query token per (b, h): q [B, H, d],
-    caches [B, H, Lkv, d], all bf16."""
-    B, H, L, d = kcache.shape
+    caches [B, Hkv, Lkv, d], all bf16 (H a multiple of Hkv: query head h
+    reads cache head h // (H // Hkv))."""
+    B, Hkv, L, d = kcache.shape
+    H = q.shape[1]
     for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
         _need(t, torch.bfloat16, n)
     o = torch.empty_like(q)
     lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if with_lse else None
-    if scale is None and not with_lse and workspace is None:
+    if Hkv != H:
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        _lib.check(_lib.fa_decode_gqa(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                      o.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                      B, H, Hkv, L, d, num_splits, scale, ws_ptr, ws_bytes,
+                                      _stream()))
+    elif scale is None and not with_lse and workspace is None:
         _lib.check(_lib.fa_decode(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
                                   o.data_ptr(), B, H, L, d, num_splits, _stream()))
     else:

@@ -123,6 +123,19 @@ int check_scale(float scale) {
   return FA_OK;
 }
 
+// Grouped heads and window: Hq = g * Hkv query heads share Hkv key/value
+// heads; window 0 means none, window >= 1 needs the causal mask.
+int check_heads(const char* fn, int Hq, int Hkv, int causal, int window) {
+  if (Hkv < 1 || Hq % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: Hq (%d) must be a positive multiple of Hkv (%d)", fn, Hq,
+                Hkv);
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (window < 0) return fail(FA_ERR_INVALID_ARG, "%s: window must be >= 0 (got %d)", fn, window);
+  if (window > 0 && !causal)
+    return fail(FA_ERR_UNSUPPORTED, "%s: a sliding window needs causal = 1", fn);
+  return FA_OK;
+}
+
 int launch_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess)
     return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -133,23 +146,36 @@ int launch_result(cudaError_t e, const char* what) {
 
 extern "C" {
 
-int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-               int N, int d, float scale, int causal, cudaStream_t stream) {
-  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "fa_forward: null pointer");
-  if (int r = check_sizes(B, H, N, d)) return r;
-  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_forward: d must be 128 (got %d)", d);
+static int forward_impl(const char* fn, const void* q, const void* k, const void* v, void* o,
+                        float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                        int causal, int window, cudaStream_t stream) {
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (int r = check_sizes(B, Hq, N, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
   if (int r = check_scale(scale)) return r;
-  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
-    return fail(FA_ERR_INVALID_ARG, "fa_forward: pointers must be 16-byte aligned");
+    return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
   fa::FwdMaps maps;
-  const int BH = B * H;
-  if (int r = make_map(&maps.q, q, BH, N, 128)) return r;
-  if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
-  if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
-  return launch_result(fa::launch_forward_bf16(maps, o, lse, B, H, N, scale, causal, stream, g_events),
-                       "fa_forward launch");
+  if (int r = make_map(&maps.q, q, B * Hq, N, 128)) return r;
+  if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
+  if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
+  return launch_result(fa::launch_forward_bf16(maps, o, lse, B, Hq, Hkv, N, scale, causal,
+                                               window >= N ? 0 : window, stream, g_events),
+                       "forward launch");
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, cudaStream_t stream) {
+  return forward_impl("fa_forward", q, k, v, o, lse, B, H, H, N, d, scale, causal, 0, stream);
+}
+
+int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int N, int d, float scale, int causal, int window,
+                   cudaStream_t stream) {
+  return forward_impl("fa_forward_gqa", q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, window,
+                      stream);
 }
 
 int fa_forward_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
@@ -172,61 +198,70 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o, fl
       "fa_forward_fp32 launch");
 }
 
-static int backward_impl(const void* q, const void* k, const void* v, const void* o,
-                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
-                         int H, int N, int d, float scale, int causal, void* ws,
-                         size_t ws_bytes, bool own_ws, cudaStream_t stream) {
+static int backward_impl(const char* fn, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                         void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                         int causal, int window, void* ws, size_t ws_bytes, bool own_ws,
+                         cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
-    return fail(FA_ERR_INVALID_ARG, "fa_backward: null pointer");
-  if (int r = check_sizes(B, H, N, d)) return r;
-  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "fa_backward: d must be 128 (got %d)", d);
+    return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (int r = check_sizes(B, Hq, N, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
   if (int r = check_scale(scale)) return r;
-  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
   const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : ptrs)
-    if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "fa_backward: pointers must be 16-byte aligned");
+    if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
   if (reinterpret_cast<uintptr_t>(lse) & 3u)
-    return fail(FA_ERR_INVALID_ARG, "fa_backward: lse must be 4-byte aligned");
-  const size_t need = fa::backward_workspace_bytes(B, H, N);
+    return fail(FA_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", fn);
+  const size_t need = fa::backward_workspace_bytes(B, Hq, N);
   if (!own_ws) {
     if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
       return fail(FA_ERR_INVALID_ARG,
-                  "fa_backward_ex: workspace must be 256-byte aligned and >= %zu bytes", need);
+                  "%s: workspace must be 256-byte aligned and >= %zu bytes", fn, need);
   }
-  const int BH = B * H;
   fa::BwdMaps maps;
-  if (int r = make_map(&maps.q, q, BH, N, 64)) return r;     // 64-query blocks
-  if (int r = make_map(&maps.dO, dO, BH, N, 64)) return r;
-  if (int r = make_map(&maps.k, k, BH, N, 128)) return r;
-  if (int r = make_map(&maps.v, v, BH, N, 128)) return r;
+  if (int r = make_map(&maps.q, q, B * Hq, N, 64)) return r;     // 64-query blocks
+  if (int r = make_map(&maps.dO, dO, B * Hq, N, 64)) return r;
+  if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
+  if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
   if (own_ws) {
     if (workspace_alloc(&ws, need, stream) != cudaSuccess) {
       cudaGetLastError();
-      return fail(FA_ERR_NO_MEMORY, "fa_backward: workspace allocation of %zu bytes failed", need);
+      return fail(FA_ERR_NO_MEMORY, "%s: workspace allocation of %zu bytes failed", fn, need);
     }
   }
-  cudaError_t e = fa::launch_backward_bf16(maps, q, k, v, o, lse, dO, dq, dk, dv, B, H, N,
-                                           scale, causal, ws, stream, g_events);
+  cudaError_t e = fa::launch_backward_bf16(maps, q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N,
+                                           scale, causal, window >= N ? 0 : window, ws, stream,
+                                           g_events);
   if (own_ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = e2;
   }
-  return launch_result(e, "fa_backward launch");
+  return launch_result(e, "backward launch");
 }
 
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                 float scale, int causal, cudaStream_t stream) {
-  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, nullptr, 0,
-                       true, stream);
+  return backward_impl("fa_backward", q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale,
+                       causal, 0, nullptr, 0, true, stream);
 }
 
 int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
                    const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H,
                    int N, int d, float scale, int causal, void* ws, size_t ws_bytes,
                    cudaStream_t stream) {
-  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, ws,
-                       ws_bytes, false, stream);
+  return backward_impl("fa_backward_ex", q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale,
+                       causal, 0, ws, ws_bytes, false, stream);
+}
+
+int fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                    int Hq, int Hkv, int N, int d, float scale, int causal, int window,
+                    void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return backward_impl("fa_backward_gqa", q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d,
+                       scale, causal, window, ws, ws_bytes, ws == nullptr, stream);
 }
 
 int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
@@ -260,6 +295,52 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
     if (e == cudaSuccess) e = e2;
   }
   return launch_result(e, "fa_decode launch");
+}
+
+int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o,
+                  float* lse_out, int B, int Hq, int Hkv, int Lkv, int d, int num_splits,
+                  float scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const char* fn = "fa_decode_gqa";
+  if (!q || !kcache || !vcache || !o) return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (int r = check_sizes(B, Hq, Lkv, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
+  if (int r = check_scale(scale)) return r;
+  if (int r = check_heads(fn, Hq, Hkv, 0, 0)) return r;
+  if (num_splits < 1 || num_splits > Lkv || num_splits > 1024)
+    return fail(FA_ERR_INVALID_ARG, "%s: num_splits must be in [1, min(Lkv, 1024)] (got %d)", fn,
+                num_splits);
+  const int group = Hq / Hkv;
+  if (static_cast<long long>(B) * Hkv * ((group + 15) / 16) > 65535ll ||
+      static_cast<long long>(B) * Hq > 65535ll)
+    return fail(FA_ERR_UNSUPPORTED, "%s: B*Hq must be <= 65535", fn);
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)))
+    return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+  const size_t need = fa::decode_workspace_bytes(B, Hq, num_splits);
+  const bool own = (ws == nullptr);
+  if (!own && (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+    return fail(FA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned and >= %zu bytes",
+                fn, need);
+  CUtensorMap tk, tv;
+  if (group > 1) {
+    if (int r = make_map(&tk, kcache, B * Hkv, Lkv, 64)) return r;
+    if (int r = make_map(&tv, vcache, B * Hkv, Lkv, 64)) return r;
+  }
+  if (own && workspace_alloc(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FA_ERR_NO_MEMORY, "%s: workspace allocation of %zu bytes failed", fn, need);
+  }
+  // One query head per key/value head is plain decode (per-row kernel).
+  cudaError_t e = group == 1
+                      ? fa::launch_decode(q, kcache, vcache, o, lse_out, B, Hq, Lkv, num_splits,
+                                          scale, ws, stream, g_events)
+                      : fa::launch_decode_gqa(tk, tv, q, o, lse_out, B, Hq, Hkv, Lkv,
+                                              num_splits, scale, ws, stream, g_events);
+  if (own) {
+    cudaError_t e2 = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  return launch_result(e, "fa_decode_gqa launch");
 }
 
 int fa_decode(const void* q, const void* kcache, const void* vcache, void* o, int B, int H,

@@ -34,6 +34,13 @@
 //   bwd_convert  dQ = bf16(accumulator).
 // Causal: query blocks entirely above the key block are skipped; the blocks
 // that straddle the diagonal are masked element-wise.
+// Grouped query heads ("FlashAttention ontleed", "Interactie met de
+// KV-cache"): a thread block owns key block j of key/value head b*Hkv + t and
+// streams the query blocks of all g query heads b*Hq + t*g .. + g-1 past it,
+// so dK and dV (sums over the group) stay in TMEM until the end.
+// Sliding window ("03. FlashAttention", "Variantes et extensions"): key k is
+// seen by queries k .. k+w-1, so query blocks past the window of the key
+// block are skipped and the blocks that cut through its edge are masked.
 #include <cfloat>
 
 #include "fa_device.cuh"
@@ -183,8 +190,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const float* __restrict__ lse_pad, const float* __restrict__ d_pad,
                 float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dK,
-                __nv_bfloat16* __restrict__ dV, int BH, int N, int Npad, float scale,
-                int causal) {
+                __nv_bfloat16* __restrict__ dV, int BHkv, int N, int Npad, float scale,
+                int causal, int qgroup, int window, int head_group) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {           // the swizzled layouts need a 1024-byte aligned base
@@ -197,19 +204,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Blocks are ordered by groups of kHeadGroup heads, so the few heads in
-  // flight keep their dQ accumulator, Q and dO resident in L2; within a
-  // group, key blocks go in increasing order (most work first when causal).
+  // Blocks are ordered by groups of head_group key/value heads, so the few
+  // heads in flight keep their dQ accumulator, Q and dO resident in L2;
+  // within a group, key blocks go in increasing order (most work first when
+  // causal).
   const int nqb = (N + BQ - 1) / BQ;
   const int nkv = (N + BKV - 1) / BKV;
-  const int per_group = kHeadGroup * nkv;
-  const int group = static_cast<int>(blockIdx.x) / per_group;
-  const int gsize = min(kHeadGroup, BH - group * kHeadGroup);
-  const int rem = static_cast<int>(blockIdx.x) - group * per_group;
+  const int per_group = head_group * nkv;
+  const int hgrp = static_cast<int>(blockIdx.x) / per_group;
+  const int gsize = min(head_group, BHkv - hgrp * head_group);
+  const int rem = static_cast<int>(blockIdx.x) - hgrp * per_group;
   const int j = rem / gsize;                          // key block
-  const int bh = group * kHeadGroup + rem % gsize;
+  const int bkv = hgrp * head_group + rem % gsize;    // key/value head
   const int i0 = causal ? (j * BKV) / BQ : 0;         // first query block that sees key block j
-  const int nit = nqb - i0;
+  // last query block that sees key block j (window: key k is seen up to k+w-1)
+  const int i1 = window > 0 ? min(nqb - 1, (j * BKV + BKV - 1 + window - 1) / BQ) : nqb - 1;
+  const int nph = i1 - i0 + 1;                        // query blocks per query head
+  const int nit = qgroup * nph;                       // over the g query heads of the group
+  // iteration it -> query head bkv*g + it/nph, query block i0 + it%nph
+  auto q_head = [&](int it) { return bkv * qgroup + it / nph; };
+  auto q_start = [&](int it) { return (i0 + it % nph) * BQ; };
   const float scale_log2 = scale * kLog2e;
 
   if (threadIdx.x == 0) {
@@ -246,13 +260,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       prefetch_tmap(&tmdO);
       const uint32_t kvf = bar_addr(sbase, B_KVFULL);
       mbar_arrive_expect_tx(kvf, 2 * TILE);
-      tma_load_3d(sbase + OFF_K, &tmK, kvf, 0, j * BKV, bh);
-      tma_load_3d(sbase + OFF_K + HALF, &tmK, kvf, 64, j * BKV, bh);
-      tma_load_3d(sbase + OFF_V, &tmV, kvf, 0, j * BKV, bh);
-      tma_load_3d(sbase + OFF_V + HALF, &tmV, kvf, 64, j * BKV, bh);
+      tma_load_3d(sbase + OFF_K, &tmK, kvf, 0, j * BKV, bkv);
+      tma_load_3d(sbase + OFF_K + HALF, &tmK, kvf, 64, j * BKV, bkv);
+      tma_load_3d(sbase + OFF_V, &tmV, kvf, 0, j * BKV, bkv);
+      tma_load_3d(sbase + OFF_V + HALF, &tmV, kvf, 64, j * BKV, bkv);
       for (int it = 0; it < nit; ++it) {
         const int st = it % STAGES;
-        const int qb = (i0 + it) * BQ;
+        const int qb = q_start(it);
+        const int bh = q_head(it);
         if (it >= STAGES && !ctx.wait(B_QEMPTY + st, ((it / STAGES) - 1) & 1)) break;
         const uint32_t qf = bar_addr(sbase, B_QFULL + st);
         const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
@@ -368,13 +383,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int kv = j * BKV + row;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int qlo = causal ? kv : 0;
-    const uint32_t qspan = kv < N ? static_cast<uint32_t>(N - 1 - qlo) : 0u;
+    const int qhi = window > 0 ? min(N - 1, kv + window - 1) : N - 1;
+    const uint32_t qspan = kv < N ? static_cast<uint32_t>(qhi - qlo) : 0u;
     const bool row_valid = kv < N;
     bool ok = true;
     for (int it = 0; it < nit; ++it) {
       const int x = it & 1;
       const int st = it % STAGES;
-      const int qb = (i0 + it) * BQ;
+      const int qb = q_start(it);
       const float* stage_lse =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
@@ -388,11 +404,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         break;
       }
       tc_fence_after();
-      // Valid queries for this key row: q in [qlo, N - 1] (causal: q >= kv;
-      // past the end of the sequence nothing is valid).  Only blocks on the
-      // diagonal or at a ragged end need it; the test is block-uniform.
-      const bool need_mask =
-          (causal && qb < j * BKV + BKV) || (qb + BQ > N) || (j * BKV + BKV > N);
+      // Valid queries for this key row: q in [qlo, qhi] (causal: q >= kv;
+      // window: q <= kv + w - 1; past the end of the sequence nothing is
+      // valid).  Only blocks on the diagonal, on the window's edge or at a
+      // ragged end need it; the test is block-uniform.
+      const bool need_mask = (causal && qb < j * BKV + BKV) || (qb + BQ > N) ||
+                             (j * BKV + BKV > N) || (window > 0 && qb + BQ > j * BKV + window);
       const int col0 = sub * 32;                      // first query column of this slice
       const uint32_t s_addr = tmem + lane_addr + 128u * x + col0;
       uint32_t sr[32], dr[32];
@@ -409,7 +426,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
         float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
         if (need_mask) {
-          // qlo <= q <= N - 1 as one unsigned compare per query (the
+          // qlo <= q <= qhi as one unsigned compare per query (the
           // wrap-around of rel + t is the exact difference mod 2^32)
           const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
           p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
@@ -454,7 +471,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tmem_ld32(src + c * 32, r);
         if (kv < N) {
           uint4* d4 =
-              reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + kv) * HD + c * 32);
+              reinterpret_cast<uint4*>(out + (static_cast<size_t>(bkv) * N + kv) * HD + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             d4[i] = make_uint4(
@@ -471,7 +488,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
     for (int it = 0; it < nit; ++it) {
       const int x = it & 1;
-      const int qb = (i0 + it) * BQ;
+      const int qb = q_start(it);
+      const int bh = q_head(it);
       if (!ctx.wait(B_DQFULL + x, (it >> 1) & 1)) break;
       tc_fence_after();
       float g[BQ];
@@ -522,7 +540,7 @@ size_t backward_workspace_bytes(int B, int H, int N) {
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H,
-                                 int N, float scale, int causal, void* ws,
+                                 int Hkv, int N, float scale, int causal, int window, void* ws,
                                  cudaStream_t stream, const TimingEvents& ev) {
   (void)q;
   (void)k;
@@ -551,9 +569,11 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   if (e != cudaSuccess) return e;
   const int nkv = (N + BKV - 1) / BKV;
   if (ev.before) cudaEventRecord(ev.before, stream);
-  bwd_main_kernel<<<dim3(nkv * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
+  const int g = H / Hkv;
+  const int head_group = max(1, kHeadGroup / g);   // about kHeadGroup query heads in flight
+  bwd_main_kernel<<<dim3(nkv * B * Hkv), dim3(NTHREADS), SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.dO, lse_pad, d_pad, dq_acc, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), BH, N, Npad, scale, causal);
+      static_cast<__nv_bfloat16*>(dv), B * Hkv, N, Npad, scale, causal, g, window, head_group);
   e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;

@@ -23,12 +23,13 @@ cudaError_t launch_forward_fp32(const float* q, const float* k, const float* v, 
 int status_forward_fp32(bool clear);
 
 // ---- bf16 tcgen05 forward (fwd_bf16.cu); tensor maps over [B*H, N, 128]
+// (Q) and [B*Hkv, N, 128] (K, V); window 0 = none.
 struct FwdMaps {
   CUtensorMap q, k, v;
 };
 cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
-                                int N, float scale, int causal, cudaStream_t stream,
-                                const TimingEvents& ev);
+                                int Hkv, int N, float scale, int causal, int window,
+                                cudaStream_t stream, const TimingEvents& ev);
 int status_forward_bf16(bool clear);
 
 // ---- bf16 backward (bwd_bf16.cu)
@@ -36,10 +37,11 @@ struct BwdMaps {
   CUtensorMap q, k, v, dO;
 };
 size_t backward_workspace_bytes(int B, int H, int N);
+// Q, dO, O, LSE, dQ have H query heads; K, V, dK, dV have Hkv (H % Hkv == 0).
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H,
-                                 int N, float scale, int causal, void* ws,
+                                 int Hkv, int N, float scale, int causal, int window, void* ws,
                                  cudaStream_t stream, const TimingEvents& ev);
 int status_backward_bf16(bool clear);
 
@@ -49,6 +51,12 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
                           float* lse_out, int B, int H, int L, int num_splits, float scale,
                           void* ws, cudaStream_t stream, const TimingEvents& ev);
 int status_decode(bool clear);
+// Grouped heads (Hq = g * Hkv): tensor maps over the caches [B*Hkv, L, 128]
+// with 64-row boxes; partials and workspace as launch_decode with H = Hq.
+cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q,
+                              void* o, float* lse_out, int B, int Hq, int Hkv, int L,
+                              int num_splits, float scale, void* ws, cudaStream_t stream,
+                              const TimingEvents& ev);
 
 // Fixed device scratch of fa_decode_noalloc (decode.cu): room for
 // kNoAllocMaxParts = B * H * num_splits partial results.

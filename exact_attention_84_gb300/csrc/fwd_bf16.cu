@@ -36,6 +36,15 @@
 // Causal: key tiles above the diagonal are skipped; only diagonal tiles (and
 // a ragged last tile) are masked element-wise.  Heavy (late) Q blocks are
 // scheduled first.
+// Grouped query heads ("FlashAttention ontleed", "Interactie met de
+// KV-cache": several query heads share one key/value head): query head
+// b*Hq + h reads key/value head b*Hkv + h/g, which is (b*Hq + h) / g since
+// Hq = g*Hkv; consecutive thread blocks take consecutive query heads, so the
+// g heads of a group read the same K/V tiles close together in time (L2).
+// Sliding window ("03. FlashAttention", "Variantes et extensions": only keys
+// inside the window): query i sees keys i-w+1 .. i.  Each Q block starts at
+// the first key tile that any of its rows sees; tiles that cut through the
+// window's lower edge are masked element-wise like diagonal tiles.
 #include <cfloat>
 
 #include "fa_device.cuh"
@@ -131,7 +140,8 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, uint32_t tmem, int blk, u
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                float* __restrict__ LSE, int BH, int N, float scale_log2, int causal) {
+                float* __restrict__ LSE, int BH, int N, float scale_log2, int causal,
+                int group, int window) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -148,9 +158,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int pair = causal ? (npair - 1 - static_cast<int>(blockIdx.x) / BH)
                           : (static_cast<int>(blockIdx.x) / BH);
   const int bh = static_cast<int>(blockIdx.x) % BH;
-  // key tiles needed by Q block A (tile 2*pair) and B (tile 2*pair + 1)
+  const int bkv = bh / group;                   // key/value head of this query head
+  // key tiles [lo, nt) needed by Q block A (tile 2*pair) and B (tile 2*pair + 1)
   const int ntA = causal ? min(2 * pair + 1, nkv) : nkv;
   const int ntB = causal ? min(2 * pair + 2, nkv) : nkv;
+  const int loA = window > 0 ? max(0, 2 * pair * BM - window + 1) / BN : 0;
+  const int loB = window > 0 ? min(max(0, (2 * pair + 1) * BM - window + 1) / BN, ntB - 1) : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(sbase, B_QFULL), 1);
@@ -190,7 +203,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_load_3d(sbase + OFF_QB + HALF_BYTES, &tmQ, qf, 64, q0 + BM, bh);
       bool ok = true;
       int cnt = 0;
-      for (int j = 0; j < ntB && ok; ++j) {
+      for (int j = loA; j < ntB && ok; ++j) {
         for (int which = 0; which < 2 && ok; ++which, ++cnt) {
           const int slot = cnt % SLOTS;
           if (cnt >= SLOTS && !ctx.wait(B_EMPTY + slot, ((cnt / SLOTS) - 1) & 1)) {
@@ -201,8 +214,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           const uint32_t dst = sbase + OFF_SLOT + slot * TILE_BYTES;
           const CUtensorMap* map = which ? &tmV : &tmK;
           mbar_arrive_expect_tx(fb, TILE_BYTES);
-          tma_load_3d(dst, map, fb, 0, j * BN, bh);
-          tma_load_3d(dst + HALF_BYTES, map, fb, 64, j * BN, bh);
+          tma_load_3d(dst, map, fb, 0, j * BN, bkv);
+          tma_load_3d(dst + HALF_BYTES, map, fb, 64, j * BN, bkv);
         }
       }
     }
@@ -210,34 +223,46 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // K_j sits in slot (2j) % SLOTS, V_j in (2j+1) % SLOTS; the n-th fill of
-      // a slot completes phase n of its FULL barrier.
-      auto full_k = [&](int j) { return ctx.wait(B_FULL + (2 * j) % SLOTS, ((2 * j) / SLOTS) & 1); };
-      auto full_v = [&](int j) {
-        return ctx.wait(B_FULL + (2 * j + 1) % SLOTS, ((2 * j + 1) / SLOTS) & 1);
+      // Tiles are numbered from loA: K_j sits in slot (2t) % SLOTS and V_j in
+      // (2t+1) % SLOTS with t = j - loA; the n-th fill of a slot completes
+      // phase n of its FULL barrier.  Block A works on tiles [loA, ntA) and
+      // block B on [loB, ntB), with loB <= loA + 1 and ntB >= ntA, so B takes
+      // every tile after the first.
+      auto full_k = [&](int j) {
+        const int t = j - loA;
+        return ctx.wait(B_FULL + (2 * t) % SLOTS, ((2 * t) / SLOTS) & 1);
       };
-      bool ok = ctx.wait(B_QFULL, 0) && full_k(0);
+      auto full_v = [&](int j) {
+        const int t = j - loA;
+        return ctx.wait(B_FULL + (2 * t + 1) % SLOTS, ((2 * t + 1) / SLOTS) & 1);
+      };
+      auto active_a = [&](int j) { return j < ntA; };
+      auto active_b = [&](int j) { return j >= loB; };
+      bool ok = ctx.wait(B_QFULL, 0) && full_k(loA);
       if (ok) {
         tc_fence_after();
         issue_s(ctx, tmem, 0, 0);
         mma_commit(bar_addr(sbase, B_SFULL + 0));
-        issue_s(ctx, tmem, 1, 0);
-        mma_commit(bar_addr(sbase, B_SFULL + 1));
+        if (active_b(loA)) {
+          issue_s(ctx, tmem, 1, 0);
+          mma_commit(bar_addr(sbase, B_SFULL + 1));
+        }
         mma_commit(bar_addr(sbase, B_EMPTY + 0));
       }
-      for (int j = 0; j < ntB && ok; ++j) {
-        const int vslot = (2 * j + 1) % SLOTS;
-        const int kslot_next = (2 * j + 2) % SLOTS;
+      for (int j = loA; j < ntB && ok; ++j) {
+        const int t = j - loA;
+        const int vslot = (2 * t + 1) % SLOTS;
+        const int kslot_next = (2 * t + 2) % SLOTS;
         bool v_ready = false, k_next_ready = false;
-        if (j < ntA) {
-          ok = ctx.wait(B_PFULL + 0, j & 1) && full_v(j);
+        if (active_a(j)) {
+          ok = ctx.wait(B_PFULL + 0, (j - loA) & 1) && full_v(j);
           if (!ok) break;
           v_ready = true;
           tc_fence_after();
-          issue_pv(ctx, tmem, 0, vslot, j == 0);
+          issue_pv(ctx, tmem, 0, vslot, j == loA);
           if (j == ntA - 1) mma_commit(bar_addr(sbase, B_ODONE + 0));
         }
-        if (j + 1 < ntA) {
+        if (active_a(j + 1)) {
           ok = full_k(j + 1);
           if (!ok) break;
           k_next_ready = true;
@@ -245,12 +270,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           issue_s(ctx, tmem, 0, kslot_next);
           mma_commit(bar_addr(sbase, B_SFULL + 0));
         }
-        ok = ctx.wait(B_PFULL + 1, j & 1) && (v_ready || full_v(j));
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(ctx, tmem, 1, vslot, j == 0);
+        if (active_b(j)) {
+          ok = ctx.wait(B_PFULL + 1, (j - loB) & 1) && (v_ready || full_v(j));
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(ctx, tmem, 1, vslot, j == loB);
+          if (j == ntB - 1) mma_commit(bar_addr(sbase, B_ODONE + 1));
+        }
         mma_commit(bar_addr(sbase, B_EMPTY + vslot));
-        if (j == ntB - 1) mma_commit(bar_addr(sbase, B_ODONE + 1));
         if (j + 1 < ntB) {
           ok = k_next_ready || full_k(j + 1);
           if (!ok) break;
@@ -270,6 +297,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int qt = 2 * pair + blk;                // Q tile index (128-row units)
     const int q_row = qt * BM + row;
     const int nt = blk ? ntB : ntA;
+    const int lo = blk ? loB : loA;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * blk;
     const uint32_t o_addr = tmem + lane_addr + TM_O + 128 * blk;
@@ -277,8 +305,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     float l = 0.f;                                // running sum
     bool ok = true;
 
-    for (int j = 0; j < nt; ++j) {
-      if (!ctx.wait(B_SFULL + blk, j & 1)) {
+    for (int j = lo; j < nt; ++j) {
+      if (!ctx.wait(B_SFULL + blk, (j - lo) & 1)) {
         ok = false;
         break;
       }
@@ -290,14 +318,21 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
       }
-      // mask: causal diagonal tile, or keys past the end of the sequence
+      // mask: causal diagonal tile, keys past the end of the sequence, or a
+      // tile that cuts through the window's lower edge
       const bool diag = causal && (j == qt);
       const bool ragged = (j == nkv - 1) && (N % BN != 0);
-      if (diag || ragged) {
-        const int lim = causal ? min(q_row, N - 1) : (N - 1);
+      const bool wedge = window > 0 && j * BN < qt * BM + BM - window;
+      if (diag || ragged || wedge) {
+        // keys visible to this row: key_lo <= key <= key_hi, tested as one
+        // unsigned compare per key
+        const int key_hi = causal ? min(q_row, N - 1) : (N - 1);
+        const int key_lo = window > 0 ? q_row - window + 1 : 0;
+        const uint32_t span = static_cast<uint32_t>(key_hi - key_lo);
+        const int rel0 = j * BN - key_lo;
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (j * BN + c > lim) s[c] = -INFINITY;
+          if (static_cast<uint32_t>(rel0 + c) > span) s[c] = -INFINITY;
       }
       float mx = -INFINITY;
 #pragma unroll
@@ -310,13 +345,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         corr = fast_exp2(m - mx);                 // 0 on the first tile
         m = mx;
       }
-      const bool rescale_o = (j > 0) && __any_sync(0xffffffffu, corr != 1.f);
+      const bool rescale_o = (j > lo) && __any_sync(0xffffffffu, corr != 1.f);
+      // A row that has seen no visible key yet (only possible with a window)
+      // keeps m = -inf; it uses 0 as the exponent reference so its masked
+      // scores give exp2(-inf) = 0, not NaN.
+      const float mref = (m == -INFINITY) ? 0.f : m;
       float rs = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -m));
-        const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -m));
+        const float p0 = fast_exp2(fmaf(s[2 * c], scale_log2, -mref));
+        const float p1 = fast_exp2(fmaf(s[2 * c + 1], scale_log2, -mref));
         rs += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
@@ -375,8 +414,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }  // namespace
 
 cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
-                                int N, float scale, int causal, cudaStream_t stream,
-                                const TimingEvents& ev) {
+                                int Hkv, int N, float scale, int causal, int window,
+                                cudaStream_t stream, const TimingEvents& ev) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel,
@@ -390,7 +429,8 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
   const float scale_log2 = scale * 1.4426950408889634f;
   if (ev.before) cudaEventRecord(ev.before, stream);
   fwd_bf16_kernel<<<dim3(npair * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
-      maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal);
+      maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal,
+      H / Hkv, window);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;

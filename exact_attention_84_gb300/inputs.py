@@ -28,6 +28,12 @@ class Workload:
     causal: bool = False
     kind: str = "forward"        # forward | train | decode
     uniform_head: int | None = None   # head whose K rows all equal its row 0
+    Hkv: int | None = None       # key/value heads (grouped query heads); None: H
+    window: int = 0              # causal sliding window width; 0: none
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
 
 
 # The synthetic workloads, by what they are.
@@ -39,7 +45,15 @@ TRAIN_N4096 = Workload("bf16 causal forward+backward B8 H32 N4096 d128", 8, 32, 
                        torch.bfloat16, 3, causal=True, kind="train")
 DECODE_L32K = Workload("bf16 split-KV decode B64 H32 Lkv32768 d128", 64, 32, 32768, 128,
                        torch.bfloat16, 4, kind="decode")
-ALL = [TINY_FP32, FWD_N2048, LONG_CAUSAL, TRAIN_N4096, DECODE_L32K]
+# Grouped query heads (4 query heads per key/value head) and a sliding window.
+GQA_TRAIN_N4096 = Workload("bf16 causal GQA forward+backward B8 Hq32 Hkv8 N4096 d128", 8, 32,
+                           4096, 128, torch.bfloat16, 5, causal=True, kind="train", Hkv=8)
+WINDOW_N8192 = Workload("bf16 causal sliding-window (w=1024) forward B1 H32 N8192 d128", 1, 32,
+                        8192, 128, torch.bfloat16, 6, causal=True, window=1024)
+GQA_DECODE_L32K = Workload("bf16 GQA split-KV decode B64 Hq32 Hkv8 Lkv32768 d128", 64, 32,
+                           32768, 128, torch.bfloat16, 7, kind="decode", Hkv=8)
+ALL = [TINY_FP32, FWD_N2048, LONG_CAUSAL, TRAIN_N4096, DECODE_L32K, GQA_TRAIN_N4096,
+       WINDOW_N8192, GQA_DECODE_L32K]
 
 
 def _draw(g, shape_per_batch, B, dtype, device):
@@ -70,6 +84,26 @@ def attention_inputs(B, H, N, d, dtype, seed, device, with_do=False, uniform_hea
     return q, k, v
 
 
+def gqa_inputs(B, Hq, Hkv, N, d, dtype, seed, device, with_do=False):
+    """q [B, Hq, N, d], k, v [B, Hkv, N, d] (and dO [B, Hq, N, d])."""
+    g = generator(seed, device)
+    q = _draw(g, (Hq, N, d), B, dtype, device)
+    k = _draw(g, (Hkv, N, d), B, dtype, device)
+    v = _draw(g, (Hkv, N, d), B, dtype, device)
+    if with_do:
+        return q, k, v, _draw(g, (Hq, N, d), B, dtype, device)
+    return q, k, v
+
+
+def decode_gqa_inputs(B, Hq, Hkv, L, d, dtype, seed, device):
+    """q [B, Hq, d] and contiguous caches [B, Hkv, L, d]."""
+    g = generator(seed, device)
+    q = _draw(g, (Hq, d), B, dtype, device)
+    kc = _draw(g, (Hkv, L, d), B, dtype, device)
+    vc = _draw(g, (Hkv, L, d), B, dtype, device)
+    return q, kc, vc
+
+
 def decode_inputs(B, H, L, d, dtype, seed, device):
     """q [B, H, d] and contiguous caches [B, H, L, d]."""
     g = generator(seed, device)
@@ -80,6 +114,11 @@ def decode_inputs(B, H, L, d, dtype, seed, device):
 
 
 def workload_inputs(w: Workload, device):
+    if w.Hkv is not None:
+        if w.kind == "decode":
+            return decode_gqa_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.dtype, w.seed, device)
+        return gqa_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.dtype, w.seed, device,
+                          with_do=(w.kind == "train"))
     if w.kind == "decode":
         return decode_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, device)
     return attention_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, device,

@@ -95,6 +95,31 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o,
                     int causal, cudaStream_t stream);
 
 /*
+ * fa_forward_gqa -- fa_forward with grouped query heads and an optional
+ * causal sliding window.
+ *
+ * Grouped-query attention ("FlashAttention ontleed", "Interactie met de
+ * KV-cache": several query heads share one key head and one value head):
+ * Hq = g * Hkv query heads; query head h reads key/value head h / g.
+ * Sliding window ("03. FlashAttention", "Variantes et extensions": the
+ * tiling only visits the keys inside the window): with window w >= 1, query
+ * i sees keys i-w+1 .. i (the pages give no formula; this causal, w-wide
+ * reading is the plainest one).  Key tiles wholly outside the window are
+ * skipped, tiles that cut its edge are masked element-wise.
+ *
+ *   q, o     [B,Hq,N,d] bf16;  k, v [B,Hkv,N,d] bf16;  lse [B,Hq,N] fp32
+ *            (may be NULL).
+ *   Hkv      >= 1 and Hq % Hkv == 0 (Hkv == Hq is fa_forward).
+ *   window   0: none.  >= 1 needs causal == 1 (FA_ERR_UNSUPPORTED
+ *            otherwise); a window >= N is the same as none.  < 0:
+ *            FA_ERR_INVALID_ARG.
+ *   Other arguments as in fa_forward.  Allocates nothing.
+ */
+int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                   int window, cudaStream_t stream);
+
+/*
  * fa_backward -- gradients dQ, dK, dV by recomputation.
  *
  * Only O and the per-row statistic (here LSE) are kept from the forward
@@ -132,6 +157,24 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
                    int causal, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * fa_backward_gqa -- fa_backward with grouped query heads and an optional
+ * causal sliding window (same meaning as in fa_forward_gqa).  dK and dV of a
+ * key/value head are the sums of the gradients of its g query heads.
+ *
+ *   q, o, dO, dq  [B,Hq,N,d] bf16;  k, v, dk, dv [B,Hkv,N,d] bf16;
+ *   lse           [B,Hq,N] fp32 from fa_forward_gqa with the same arguments.
+ *   ws            NULL: the workspace comes from the library pool as in
+ *                 fa_backward; otherwise a caller-owned device buffer of
+ *                 ws_bytes >= fa_workspace_size(FA_OP_BACKWARD, B, Hq, N, d, 0)
+ *                 bytes, 256-byte aligned, and nothing is allocated.
+ *   Other arguments as in fa_backward.
+ */
+int fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                    int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                    int window, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * fa_decode -- split-KV attention of one new query token per sequence over
  * its KV cache (FlashDecoding: "FlashAttention ontleed", "Interactie met de
  * KV-cache"; "03. FlashAttention", "Variantes et extensions"; Lensa ML FAQ
@@ -166,6 +209,23 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
                  float scale, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * fa_decode_gqa -- fa_decode_ex with grouped query heads: the g = Hq / Hkv
+ * query rows that share a key/value head are computed together, so every
+ * cache row is read from memory once for all of them ("FlashAttention
+ * ontleed", "Interactie met de KV-cache").
+ *
+ *   q, o      [B,Hq,d] bf16;  kcache, vcache [B,Hkv,Lkv,d] bf16;
+ *   lse_out   [B,Hq] fp32 or NULL.
+ *   Hkv >= 1, Hq % Hkv == 0, B*Hq <= 65535.  Splits, scale and workspace as
+ *   in fa_decode_ex, with the workspace sized by
+ *   fa_workspace_size(FA_OP_DECODE, B, Hq, Lkv, d, num_splits).
+ */
+int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o,
+                  float* lse_out, int B, int Hq, int Hkv, int Lkv, int d,
+                  int num_splits, float scale, void* ws, size_t ws_bytes,
+                  cudaStream_t stream);
+
+/*
  * fa_decode_noalloc -- fa_decode_ex without any allocation.  The pages have
  * no counterpart: this entry point exists for callers that cannot allocate
  * device memory themselves or let a library do it, e.g. a plugin running
@@ -193,6 +253,7 @@ int fa_decode_noalloc(const void* q, const void* kcache, const void* vcache,
 /*
  * fa_workspace_size -- device workspace bytes needed by an operation.
  *   op           FA_OP_FORWARD (always 0), FA_OP_BACKWARD or FA_OP_DECODE.
+ *   H            the number of query heads (Hq for the _gqa calls).
  *   n_or_lkv     N for forward/backward, Lkv for decode.
  *   num_splits   decode only; ignored otherwise.
  * Returns 0 for invalid arguments.

@@ -35,3 +35,14 @@ def test_flop_conventions():
     assert acc.backward_flops(8, 32, 4096, 128, True) == 2.5 * acc.forward_flops(8, 32, 4096,
                                                                                    128, True)
     assert math.isclose(acc.decode_kv_bytes(64, 32, 32768, 128), 34.359738368e9)
+
+
+def test_visible_pairs_brute_force():
+    """The closed form of the visible (query, key) count against a direct
+    count of the mask."""
+    for n in (1, 5, 17, 64):
+        for causal, window in ((False, 0), (True, 0), (True, 1), (True, 3), (True, 16),
+                               (True, 100)):
+            count = sum(1 for i in range(n) for j in range(n)
+                        if (not causal or j <= i) and (not window or j > i - window))
+            assert acc.visible_pairs(n, causal, window) == count
