@@ -18,7 +18,11 @@ The same line carries:
   targets       the forward kernel alone on "bf16 causal forward B1 H32 N8192"
                 and on "bf16 forward B4 H16 N2048" (causal and not), against
                 the burst bf16 peak, and split-KV decode on "B64 H32 Lkv32768"
-                in KV GB/s against the measured HBM copy bandwidth;
+                in KV GB/s against the measured HBM copy bandwidth; then the
+                grouped-query forward and backward kernels (B8 Hq32 Hkv8
+                N4096 causal), the causal sliding-window forward (w = 1024,
+                B1 H32 N8192) and grouped-query decode (B64 Hq32 Hkv8
+                Lkv32768);
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload;
   clocks        SM clocks and throttle reasons sampled during the timed loop.
 
@@ -443,6 +447,71 @@ def measure_targets(args, dev, peaks, peak_src):
     out["decode_B64_H32_L32768"] = dict(best, peak=hbm, unit="GB/s",
                                         peak_kind=f"HBM copy ({peak_src})",
                                         bytes_per_launch=acc.decode_kv_bytes(w.B, w.H, w.N, w.d))
+    del q, kc, vc, o
+
+    # grouped query heads (4 per key/value head): forward and backward kernels
+    w = inputs.GQA_TRAIN_N4096
+    q, k, v, do = inputs.workload_inputs(w, dev)
+    hkv, scale = w.kv_heads, 1 / math.sqrt(w.d)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_workspace_size(_lib.FA_OP_BACKWARD, w.B, w.H, w.N, w.d, 0),
+                     dtype=torch.uint8, device=dev)
+    fwd = lambda: _lib.check(_lib.fa_forward_gqa(  # noqa: E731
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, hkv,
+        w.N, w.d, scale, 1, 0, sh))
+    bwd = lambda: _lib.check(_lib.fa_backward_gqa(  # noqa: E731
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, hkv, w.N, w.d, scale, 1, 0,
+        ws.data_ptr(), ws.numel(), sh))
+    fl = acc.forward_flops(w.B, w.H, w.N, w.d, True)
+    for key, call, flops in (("forward_gqa_causal_B8_Hq32_Hkv8_N4096", fwd, fl),
+                             ("backward_gqa_causal_B8_Hq32_Hkv8_N4096", bwd, 2.5 * fl)):
+        ms = time_kernel(call, False)
+        t = flops / (ms * 1e-3) / 1e12
+        out[key] = {"ms": round(ms, 4), "tflops": round(t, 1), "frac": round(t / burst, 4),
+                    "peak": burst, "peak_kind": f"bf16 dense, burst ({peak_src})",
+                    "l2_flush": False}
+    del q, k, v, do, o, lse, dq, dk, dv, ws
+
+    # causal sliding window: FLOPs of the visible (query, key) pairs only
+    w = inputs.WINDOW_N8192
+    q, k, v = inputs.workload_inputs(w, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
+    ms = time_kernel(lambda: _lib.check(_lib.fa_forward_gqa(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.H,
+        w.N, w.d, 1 / math.sqrt(w.d), 1, w.window, sh)), False)
+    fl = acc.masked_forward_flops(w.B, w.H, w.N, w.d, True, w.window)
+    t = fl / (ms * 1e-3) / 1e12
+    out["forward_window1024_B1_H32_N8192"] = {
+        "ms": round(ms, 4), "tflops": round(t, 1), "frac": round(t / burst, 4), "peak": burst,
+        "peak_kind": f"bf16 dense, burst ({peak_src})", "l2_flush": False,
+        "flops": "4 d per visible (query, key) pair"}
+    del q, k, v, o, lse
+
+    # grouped-query decode: the cache (Hkv heads) read once for all query heads
+    w = inputs.GQA_DECODE_L32K
+    q, kc, vc = inputs.workload_inputs(w, dev)
+    o = torch.empty_like(q)
+    hkv = w.kv_heads
+    kv_bytes = acc.decode_kv_bytes(w.B, hkv, w.N, w.d)
+    best = None
+    for s in args.decode_splits:
+        ws = torch.empty(_lib.fa_workspace_size(_lib.FA_OP_DECODE, w.B, w.H, w.N, w.d, s),
+                         dtype=torch.uint8, device=dev)
+        ms = time_kernel(lambda: _lib.check(_lib.fa_decode_gqa(
+            q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, w.B, w.H, hkv, w.N,
+            w.d, s, 1 / math.sqrt(w.d), ws.data_ptr(), ws.numel(), sh)), False)
+        gbs = kv_bytes / (ms * 1e-3) / 1e9
+        rec = {"num_splits": s, "ms": round(ms, 4), "kv_gbs": round(gbs, 1),
+               "frac": round(gbs / hbm, 4)}
+        if best is None or gbs > best["kv_gbs"]:
+            best = rec
+    out["decode_gqa_B64_Hq32_Hkv8_L32768"] = dict(best, peak=hbm, unit="GB/s",
+                                                  peak_kind=f"HBM copy ({peak_src})",
+                                                  bytes_per_launch=kv_bytes)
     return out
 
 

@@ -221,9 +221,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int i1 = window > 0 ? min(nqb - 1, (j * BKV + BKV - 1 + window - 1) / BQ) : nqb - 1;
   const int nph = i1 - i0 + 1;                        // query blocks per query head
   const int nit = qgroup * nph;                       // over the g query heads of the group
-  // iteration it -> query head bkv*g + it/nph, query block i0 + it%nph
-  auto q_head = [&](int it) { return bkv * qgroup + it / nph; };
-  auto q_start = [&](int it) { return (i0 + it % nph) * BQ; };
+  // Iteration order: query blocks i0..i1 of query head bkv*g, then of the
+  // next head of the group, and so on; each loop walks it with a cursor.
+  struct Cursor {
+    int qi, hq;
+    __device__ void next(int lo, int hi) {
+      if (++qi > hi) {
+        qi = lo;
+        ++hq;
+      }
+    }
+  };
+  const Cursor first{i0, bkv * qgroup};
   const float scale_log2 = scale * kLog2e;
 
   if (threadIdx.x == 0) {
@@ -264,10 +273,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_load_3d(sbase + OFF_K + HALF, &tmK, kvf, 64, j * BKV, bkv);
       tma_load_3d(sbase + OFF_V, &tmV, kvf, 0, j * BKV, bkv);
       tma_load_3d(sbase + OFF_V + HALF, &tmV, kvf, 64, j * BKV, bkv);
-      for (int it = 0; it < nit; ++it) {
+      Cursor cur = first;
+      for (int it = 0; it < nit; ++it, cur.next(i0, i1)) {
         const int st = it % STAGES;
-        const int qb = q_start(it);
-        const int bh = q_head(it);
+        const int qb = cur.qi * BQ;
+        const int bh = cur.hq;
         if (it >= STAGES && !ctx.wait(B_QEMPTY + st, ((it / STAGES) - 1) & 1)) break;
         const uint32_t qf = bar_addr(sbase, B_QFULL + st);
         const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
@@ -387,10 +397,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t qspan = kv < N ? static_cast<uint32_t>(qhi - qlo) : 0u;
     const bool row_valid = kv < N;
     bool ok = true;
-    for (int it = 0; it < nit; ++it) {
+    Cursor cur = first;
+    for (int it = 0; it < nit; ++it, cur.next(i0, i1)) {
       const int x = it & 1;
       const int st = it % STAGES;
-      const int qb = q_start(it);
+      const int qb = cur.qi * BQ;
       const float* stage_lse =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
@@ -486,10 +497,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // ------------------------------------------------------------ dQ writers
     const int quad = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
-    for (int it = 0; it < nit; ++it) {
+    Cursor cur = first;
+    for (int it = 0; it < nit; ++it, cur.next(i0, i1)) {
       const int x = it & 1;
-      const int qb = q_start(it);
-      const int bh = q_head(it);
+      const int qb = cur.qi * BQ;
+      const int bh = cur.hq;
       if (!ctx.wait(B_DQFULL + x, (it >> 1) & 1)) break;
       tc_fence_after();
       float g[BQ];

@@ -137,6 +137,9 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, uint32_t tmem, int blk, u
   mma_ts_batch8(tmem + TM_O + 128 * blk, a, b, IDESC_O, first ? 0u : 1u);
 }
 
+// kWindow: a sliding window is applied (window >= 1); the plain instantiation
+// carries none of its bookkeeping.
+template <bool kWindow>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
@@ -162,8 +165,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   // key tiles [lo, nt) needed by Q block A (tile 2*pair) and B (tile 2*pair + 1)
   const int ntA = causal ? min(2 * pair + 1, nkv) : nkv;
   const int ntB = causal ? min(2 * pair + 2, nkv) : nkv;
-  const int loA = window > 0 ? max(0, 2 * pair * BM - window + 1) / BN : 0;
-  const int loB = window > 0 ? min(max(0, (2 * pair + 1) * BM - window + 1) / BN, ntB - 1) : 0;
+  const int loA = kWindow ? max(0, 2 * pair * BM - window + 1) / BN : 0;
+  const int loB = kWindow ? min(max(0, (2 * pair + 1) * BM - window + 1) / BN, ntB - 1) : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(sbase, B_QFULL), 1);
@@ -322,12 +325,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // tile that cuts through the window's lower edge
       const bool diag = causal && (j == qt);
       const bool ragged = (j == nkv - 1) && (N % BN != 0);
-      const bool wedge = window > 0 && j * BN < qt * BM + BM - window;
+      const bool wedge = kWindow && j * BN < qt * BM + BM - window;
       if (diag || ragged || wedge) {
         // keys visible to this row: key_lo <= key <= key_hi, tested as one
         // unsigned compare per key
         const int key_hi = causal ? min(q_row, N - 1) : (N - 1);
-        const int key_lo = window > 0 ? q_row - window + 1 : 0;
+        const int key_lo = kWindow ? q_row - window + 1 : 0;
         const uint32_t span = static_cast<uint32_t>(key_hi - key_lo);
         const int rel0 = j * BN - key_lo;
 #pragma unroll
@@ -349,7 +352,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // A row that has seen no visible key yet (only possible with a window)
       // keeps m = -inf; it uses 0 as the exponent reference so its masked
       // scores give exp2(-inf) = 0, not NaN.
-      const float mref = (m == -INFINITY) ? 0.f : m;
+      const float mref = (kWindow && m == -INFINITY) ? 0.f : m;
       float rs = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
@@ -418,17 +421,19 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
                                 cudaStream_t stream, const TimingEvents& ev) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
+    for (auto fn : {fwd_bf16_kernel<false>, fwd_bf16_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(SMEM_BYTES));
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   const int BH = B * H;
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (ev.before) cudaEventRecord(ev.before, stream);
-  fwd_bf16_kernel<<<dim3(npair * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
+  auto kernel = window > 0 ? fwd_bf16_kernel<true> : fwd_bf16_kernel<false>;
+  kernel<<<dim3(npair * BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal,
       H / Hkv, window);
   cudaError_t e = cudaGetLastError();
