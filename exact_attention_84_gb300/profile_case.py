@@ -1,6 +1,6 @@
 """Run one kernel family on a profiling-sized workload, for ncu captures.
 
-    python -m exact_attention_84_gb300.profile_case {fwd,fwd_nc,bwd,decode} [--launches K]
+    python -m exact_attention_84_gb300.profile_case CASE [--launches K]
 
 Workloads (inputs larger than the 129 MB L2, a few GB on the device at most):
   fwd     bf16 causal forward B1 H32 N8192 d128 (the long-context workload itself)
@@ -9,6 +9,12 @@ Workloads (inputs larger than the 129 MB L2, a few GB on the device at most):
           workload's heads; its traffic scales with the heads)
   decode  bf16 split-KV decode B4 H32 Lkv32768 d128, 8 splits (1/16 of the
           decode workload's sequences)
+  fwd_win bf16 causal sliding-window (w=1024) forward B1 H32 N8192 d128 (the
+          windowed workload itself)
+  bwd_gqa bf16 causal GQA backward B2 Hq32 Hkv8 N4096 d128 (a quarter of the
+          GQA training workload)
+  dec_gqa bf16 GQA split-KV decode B4 Hq32 Hkv8 Lkv32768 d128, 8 splits (1/16
+          of the GQA decode workload's sequences)
 One warm-up launch precedes the K profiled ones.  Prints the mean device
 time per launch measured with CUDA events (not a bench value under ncu).
 """
@@ -31,7 +37,8 @@ def main():
     from exact_attention_84_gb300 import _lib, inputs
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["fwd", "fwd_nc", "bwd", "decode"])
+    ap.add_argument("case", choices=["fwd", "fwd_nc", "bwd", "decode", "fwd_win", "bwd_gqa",
+                                     "dec_gqa"])
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
@@ -63,6 +70,42 @@ def main():
                                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
                                            dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, 1,
                                            ws.data_ptr(), nbytes, sh))
+    elif a.case == "fwd_win":
+        B, H, N, W = 1, 32, 8192, 1024
+        q, k, v = inputs.attention_inputs(B, H, N, d, torch.bfloat16, 6, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+
+        def call():
+            _lib.check(_lib.fa_forward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                           lse.data_ptr(), B, H, H, N, d, scale, 1, W, sh))
+    elif a.case == "bwd_gqa":
+        B, Hq, Hkv, N = 2, 32, 8, 4096
+        q, k, v, do = inputs.gqa_inputs(B, Hq, Hkv, N, d, torch.bfloat16, 5, dev, with_do=True)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), device=dev, dtype=torch.float32)
+        _lib.check(_lib.fa_forward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), B, Hq, Hkv, N, d, scale, 1, 0, sh))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        nbytes = _lib.fa_workspace_size(_lib.FA_OP_BACKWARD, B, Hq, N, d, 0)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def call():
+            _lib.check(_lib.fa_backward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq,
+                                            Hkv, N, d, scale, 1, 0, ws.data_ptr(), nbytes, sh))
+    elif a.case == "dec_gqa":
+        B, Hq, Hkv, L, S = 4, 32, 8, 32768, 8
+        q, kc, vc = inputs.decode_gqa_inputs(B, Hq, Hkv, L, d, torch.bfloat16, 7, dev)
+        o = torch.empty_like(q)
+        nbytes = _lib.fa_workspace_size(_lib.FA_OP_DECODE, B, Hq, L, d, S)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def call():
+            _lib.check(_lib.fa_decode_gqa(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
+                                          None, B, Hq, Hkv, L, d, S, scale, ws.data_ptr(), nbytes,
+                                          sh))
     else:
         B, H, L, S = 4, 32, 32768, 8
         q, kc, vc = inputs.decode_inputs(B, H, L, d, torch.bfloat16, 4, dev)
