@@ -20,7 +20,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_NO_MEMORY = 5
-FA_OP_FORWARD, FA_OP_BACKWARD, FA_OP_DECODE = 0, 1, 2
+FA_OP_FORWARD, FA_OP_BACKWARD, FA_OP_DECODE, FA_OP_FORWARD_FP8 = 0, 1, 2, 3
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -32,6 +32,8 @@ SIGNATURES = {
     "fa_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_forward_fp32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_forward_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_forward_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I,
+                            _P, _Z, _P]),
     "fa_backward_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
                              _I, _P, _Z, _P]),
     "fa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P]),
@@ -93,6 +95,12 @@ def fa_forward_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
 def fa_forward_gqa(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, window, stream):
     return _call("fa_forward_gqa", q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, window,
                  stream)
+
+
+def fa_forward_fp8(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, q_descale, k_descale, v_descale,
+                   causal, window, ws, ws_bytes, stream):
+    return _call("fa_forward_fp8", q, k, v, o, lse, B, Hq, Hkv, N, d, scale, q_descale,
+                 k_descale, v_descale, causal, window, ws, ws_bytes, stream)
 
 
 def fa_backward_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window,

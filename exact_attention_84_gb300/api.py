@@ -52,6 +52,27 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     return o, lse
 
 
+def forward_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float,
+                causal: bool = False, scale: float | None = None, window: int = 0, out=None,
+                lse=None, workspace=None):
+    """O (bf16), LSE for E4M3 inputs held as uint8 codes: q8 [B, H, N, d],
+    k8, v8 [B, Hkv, N, d]; real values are code * descale."""
+    B, H, N, d = q8.shape
+    Hkv = k8.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _need(t, torch.uint8, n)
+    o = torch.empty(q8.shape, device=q8.device, dtype=torch.bfloat16) if out is None else out
+    lse = torch.empty((B, H, N), device=q8.device, dtype=torch.float32) if lse is None else lse
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _lib.check(_lib.fa_forward_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, Hkv, N, d, scale, q_descale, k_descale,
+                                   v_descale, int(causal), int(window), ws_ptr, ws_bytes,
+                                   _stream()))
+    return o, lse
+
+
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
              workspace=None, out=None, window: int = 0):
     """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``.

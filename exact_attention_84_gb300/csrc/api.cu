@@ -3,7 +3,7 @@
 // Every entry point validates its arguments before anything is enqueued,
 // builds the TMA tensor maps it needs on the host, obtains workspace
 // (caller-owned, or from a library-owned stream-ordered pool), and
-// launches the kernels of fwd_fp32.cu, fwd_bf16.cu, bwd_bf16.cu and
+// launches the kernels of fwd_fp32.cu, fwd_tc.cu, bwd_bf16.cu and
 // decode.cu on the caller's stream.
 #include <cmath>
 #include <cstdarg>
@@ -70,6 +70,26 @@ int make_map(CUtensorMap* map, const void* base, int BH, int N, int box_rows) {
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return FA_OK;
+}
+
+// 3-D map over an 8-bit tensor [heads, rows, inner] with rows `stride` bytes
+// apart; boxes of 128 bytes (the swizzle span) by `box_rows` rows of one
+// head.  Elements past `inner` or `rows` read as zero.
+int make_map_u8(CUtensorMap* map, const void* base, int heads, int rows, int inner,
+                size_t stride, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride),
+                                 static_cast<cuuint64_t>(stride) * rows};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
   return FA_OK;
@@ -176,6 +196,52 @@ int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* 
                    cudaStream_t stream) {
   return forward_impl("fa_forward_gqa", q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, window,
                       stream);
+}
+
+int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int N, int d, float scale, float q_descale, float k_descale,
+                   float v_descale, int causal, int window, void* ws, size_t ws_bytes,
+                   cudaStream_t stream) {
+  const char* fn = "fa_forward_fp8";
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (int r = check_sizes(B, Hq, N, d)) return r;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
+  if (int r = check_scale(scale)) return r;
+  for (float x : {q_descale, k_descale, v_descale})
+    if (!std::isfinite(x) || !(x > 0.f))
+      return fail(FA_ERR_INVALID_ARG, "%s: descale factors must be finite and > 0", fn);
+  if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+  if (static_cast<long long>(N) > 65535ll * 64 || static_cast<long long>(B) * Hkv > 65535ll)
+    return fail(FA_ERR_UNSUPPORTED, "%s: N or B*Hkv too large", fn);
+  const size_t need = fa::forward_fp8_workspace_bytes(B, Hkv, N);
+  const bool own = (ws == nullptr);
+  if (!own && (ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+    return fail(FA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned and >= %zu bytes",
+                fn, need);
+  if (own && workspace_alloc(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FA_ERR_NO_MEMORY, "%s: workspace allocation of %zu bytes failed", fn, need);
+  }
+  fa::FwdMaps maps;
+  int r = make_map_u8(&maps.q, q, B * Hq, N, 128, 128, 128);
+  if (r == FA_OK) r = make_map_u8(&maps.k, k, B * Hkv, N, 128, 128, 128);
+  if (r == FA_OK) r = make_map_u8(&maps.v, ws, B * Hkv, 128, N, fa::fp8_vt_ld(N), 128);
+  cudaError_t e = cudaSuccess;
+  if (r == FA_OK) {
+    e = fa::launch_transpose_v_fp8(v, ws, B, Hkv, N, stream);
+    if (e == cudaSuccess)
+      e = fa::launch_forward_fp8(maps, o, lse, B, Hq, Hkv, N, scale, q_descale, k_descale,
+                                 v_descale, causal, window >= N ? 0 : window, stream, g_events);
+  }
+  if (own) {
+    cudaError_t e2 = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (r != FA_OK) return r;
+  return launch_result(e, "fa_forward_fp8 launch");
 }
 
 int fa_forward_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
@@ -387,6 +453,7 @@ size_t fa_workspace_size(int op, int B, int H, int n_or_lkv, int d, int num_spli
   if (B < 1 || H < 1 || n_or_lkv < 1 || d != 128) return 0;
   switch (op) {
     case FA_OP_FORWARD: return 0;
+    case FA_OP_FORWARD_FP8: return fa::forward_fp8_workspace_bytes(B, H, n_or_lkv);
     case FA_OP_BACKWARD: return fa::backward_workspace_bytes(B, H, n_or_lkv);
     case FA_OP_DECODE:
       if (num_splits < 1 || num_splits > n_or_lkv || num_splits > 1024) return 0;

@@ -219,6 +219,44 @@ __device__ __forceinline__ void mma_ts_batch4(uint32_t d, const uint32_t (&a)[4]
       : "memory");
 }
 
+// kind::f8f6f4 (8-bit inputs, fp32 accumulator), 4 consecutive k-steps of
+// 32 from one asm statement; both operands in shared memory.
+__device__ __forceinline__ void mma_f8_ss_batch4(uint32_t d, const uint64_t (&a)[4],
+                                                 const uint64_t (&b)[4], uint32_t idesc,
+                                                 uint32_t accumulate_first) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %9, t;\n\t"
+      "}"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]),
+        "l"(b[3]), "r"(idesc), "r"(accumulate_first)
+      : "memory");
+}
+
+// kind::f8f6f4, 4 consecutive k-steps of 32 with A in tensor memory (four
+// 8-bit elements per 32-bit column, 32 elements = 8 columns per step).
+__device__ __forceinline__ void mma_f8_ts_batch4(uint32_t d, const uint32_t (&a)[4],
+                                                 const uint64_t (&b)[4], uint32_t idesc,
+                                                 uint32_t accumulate_first) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.eq.b32 t, %10, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %5, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%2], %6, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %7, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %8, %9, t;\n\t"
+      "}"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]),
+        "l"(b[3]), "r"(idesc), "r"(accumulate_first)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -317,12 +355,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool a_mn_major,
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0 in
+// bits 7-9 and 10-12), both K-major, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- misc
 // Two fp32 values -> packed bf16 pair (round to nearest even); `lo` lands
 // in the low 16 bits.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four fp32 values -> four e4m3 bytes (round to nearest even, saturating to
+// +-448); p0 lands in the lowest byte.  Each cvt puts its first source in
+// the upper byte of the 16-bit result.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
   return r;
 }
 

@@ -22,7 +22,7 @@ cudaError_t launch_forward_fp32(const float* q, const float* k, const float* v, 
                                 int causal, cudaStream_t stream, const TimingEvents& ev);
 int status_forward_fp32(bool clear);
 
-// ---- bf16 tcgen05 forward (fwd_bf16.cu); tensor maps over [B*H, N, 128]
+// ---- bf16 tcgen05 forward (fwd_tc.cu); tensor maps over [B*H, N, 128]
 // (Q) and [B*Hkv, N, 128] (K, V); window 0 = none.
 struct FwdMaps {
   CUtensorMap q, k, v;
@@ -31,6 +31,19 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
                                 int Hkv, int N, float scale, int causal, int window,
                                 cudaStream_t stream, const TimingEvents& ev);
 int status_forward_bf16(bool clear);
+
+// ---- fp8 (e4m3) tcgen05 forward (fwd_tc.cu).  maps.q, maps.k over
+// [B*H or B*Hkv, N, 128] bytes; maps.v over the transposed copy
+// V^T [B*Hkv, 128, ld] (ld = fp8_vt_ld(N)) made by launch_transpose_v_fp8
+// in a workspace of forward_fp8_workspace_bytes.
+size_t fp8_vt_ld(int N);
+size_t forward_fp8_workspace_bytes(int B, int Hkv, int N);
+cudaError_t launch_transpose_v_fp8(const void* v, void* vt, int B, int Hkv, int N,
+                                   cudaStream_t stream);
+cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, int H, int Hkv,
+                               int N, float scale, float q_descale, float k_descale,
+                               float v_descale, int causal, int window, cudaStream_t stream,
+                               const TimingEvents& ev);
 
 // ---- bf16 backward (bwd_bf16.cu)
 struct BwdMaps {

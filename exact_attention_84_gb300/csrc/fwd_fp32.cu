@@ -9,7 +9,7 @@
 // tile divides by the running sum and writes O and LSE = m + ln(l) once.
 //
 // This path serves fp32 callers (tolerance 1e-5 rules out tensor cores);
-// the bf16 tensor-core path is fwd_bf16.cu.
+// the bf16 and fp8 tensor-core paths are in fwd_tc.cu.
 #include <cfloat>
 
 #include "fa_device.cuh"

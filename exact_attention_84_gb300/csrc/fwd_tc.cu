@@ -1,0 +1,635 @@
+// fwd_tc.cu -- fused exact-attention forward on the tcgen05 tensor cores of
+// sm_103a, for bf16 and for fp8 (e4m3) inputs.
+//
+// Method ("FlashAttention ontleed", sections "Tiling en Online Softmax" and
+// "Algoritmische kern in pseudocode"; "03. FlashAttention", section
+// "FlashAttention v1", "Mecanisme"): Q blocks stay on chip while K_j / V_j
+// tiles stream past them.  Per tile and Q block:
+//   S = Q K_j^T                      (tensor cores, fp32 accumulator in TMEM)
+//   m_new = max(m, rowmax(S*scale))  (softmax warps, registers)
+//   P = exp(S*scale - m_new)         (bf16, written back into TMEM)
+//   l = l e^(m - m_new) + rowsum(P)
+//   O = diag(e^(m - m_new)) O + P V_j   (rescale in TMEM, MMA accumulates)
+// and after the last tile O / l and LSE = m + ln(l) go to HBM once.  The
+// N x N score matrix never leaves the chip (Lensa ML "FlashAttention",
+// step 3: 0 B of S written).
+//
+// GB300 mapping (the pages' A100/H100 designs are prior art only):
+//   * One thread block owns two 128-row Q blocks (A and B) that share every
+//     K/V tile.  Tiles are 128 keys; TMA streams K_j and V_j (128-byte
+//     swizzled 64-column boxes) into a 4-slot shared-memory ring.
+//   * TMEM (512 columns): S_A, S_B (128 each) and O_A, O_B (128 each).  The
+//     softmax writes P as packed bf16 over the first 64 columns of its S
+//     buffer, and the P.V product takes P straight from TMEM (A operand in
+//     tensor memory), so only V is read from shared memory for it.
+//   * Warps 0-3 run the softmax of block A, warps 4-7 that of block B (one
+//     thread per row = TMEM lane); warp 8 issues TMA; warp 9 allocates TMEM
+//     and issues every tcgen05.mma from one thread, interleaving the two
+//     blocks: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... so one block's
+//     softmax overlaps the other block's products.
+//   * The arrival of S(j) implies PV(j-1) of the same block has completed
+//     (one thread issues them in order and tcgen05.commit tracks all earlier
+//     products), so the softmax may rescale O in TMEM right then.  A row's
+//     reference maximum is only raised when the new maximum exceeds it by
+//     more than 8 (log2 units); otherwise the old reference is kept and the
+//     exponentials stay below 2^8.  O / l and LSE = m + ln(l) use the same
+//     reference, so the result is unchanged while most O rescales are skipped.
+// Causal: key tiles above the diagonal are skipped; only diagonal tiles (and
+// a ragged last tile) are masked element-wise.  Heavy (late) Q blocks are
+// scheduled first.
+// Grouped query heads ("FlashAttention ontleed", "Interactie met de
+// KV-cache": several query heads share one key/value head): query head
+// b*Hq + h reads key/value head b*Hkv + h/g, which is (b*Hq + h) / g since
+// Hq = g*Hkv; consecutive thread blocks take consecutive query heads, so the
+// g heads of a group read the same K/V tiles close together in time (L2).
+// Sliding window ("03. FlashAttention", "Variantes et extensions": only keys
+// inside the window): query i sees keys i-w+1 .. i.  Each Q block starts at
+// the first key tile that any of its rows sees; tiles that cut through the
+// window's lower edge are masked element-wise like diagonal tiles.
+// FP8 ("03. FlashAttention", "FlashAttention v3": the FP8 format as a
+// hardware lever): Q, K, V in e4m3 with per-tensor descale factors; the
+// same loop runs kind::f8f6f4 products (K = 32 per instruction, twice the
+// bf16 rate) with fp32 accumulation.  P is rounded to e4m3 (values <= 2^8
+// thanks to the lazy rescale, inside e4m3's range) and kept in TMEM as four
+// bytes per column; V is read through a transposed copy so both operands of
+// P V are K-major.  scale * q_descale * k_descale multiplies the scores and
+// v_descale the output; O is written in bf16.
+#include <cfloat>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+__device__ int g_status_fwd;
+
+constexpr int BM = 128;                 // query rows per Q block (TMEM lanes)
+constexpr int BN = 128;                 // keys per tile
+constexpr int HD = 128;                 // head dimension
+
+// Shared-memory layout for one element type: two Q blocks, a ring of K/V
+// tile slots, the mbarriers and a few words of control state.
+template <uint32_t kTileBytes, int kSlots>
+struct FwdLayout {
+  static constexpr uint32_t TILE = kTileBytes;   // one 128 x 128 tile
+  static constexpr int SLOTS = kSlots;           // K/V ring slots
+  static constexpr uint32_t OFF_QA = 0;
+  static constexpr uint32_t OFF_QB = OFF_QA + TILE;
+  static constexpr uint32_t OFF_SLOT = OFF_QB + TILE;
+  static constexpr uint32_t OFF_BAR = OFF_SLOT + SLOTS * TILE;
+  // barrier indices
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_FULL = 1;                  // + slot
+  static constexpr int B_EMPTY = B_FULL + SLOTS;    // + slot
+  static constexpr int B_SFULL = B_EMPTY + SLOTS;   // + block (A = 0, B = 1)
+  static constexpr int B_PFULL = B_SFULL + 2;       // + block
+  static constexpr int B_ODONE = B_PFULL + 2;       // + block
+  static constexpr int NBAR = B_ODONE + 2;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
+};
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0;          // + 128 * block
+constexpr uint32_t TM_O = 256;        // + 128 * block
+
+constexpr int NTHREADS = 320;
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+// ---- bf16: 128 x 128 tiles as two 64-column (128-byte) swizzled boxes.
+struct Bf16 : FwdLayout<BM * HD * 2, 4> {
+  static constexpr uint32_t HALF = TILE / 2;        // 128 rows x 64 columns
+  // S = Q K^T: A = Q (K-major), B = K tile (K-major), M = N = 128.
+  static constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
+  // O += P V: A = P (in TMEM), B = V tile, whose rows run along the
+  // reduction (key) axis with d contiguous: MN-major.
+  static constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
+  static constexpr int P_COLS = BN / 2;             // packed P: 2 keys per TMEM column
+
+  // a 128-row tile of Q or K (rows `row`.., head `head`)
+  __device__ static void load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int row,
+                                   int head) {
+    tma_load_3d(dst, map, bar, 0, row, head);
+    tma_load_3d(dst + HALF, map, bar, 64, row, head);
+  }
+  // the V tile of keys `key`.. (V itself, [keys][d])
+  __device__ static void load_v(uint32_t dst, const CUtensorMap* map, uint32_t bar, int key,
+                                int head) {
+    load_rows(dst, map, bar, key, head);
+  }
+  // S = Q K^T: 8 k-steps of 16 along d, both operands K-major.
+  __device__ static void issue_s(uint32_t d, uint32_t q_smem, uint32_t k_smem) {
+    const uint64_t qd = sdesc_sw128(q_smem, 16, 1024);
+    const uint64_t kd = sdesc_sw128(k_smem, 16, 1024);
+    uint64_t a[8], b[8];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint64_t off = ((kk >> 2) * HALF + (kk & 3) * 32) >> 4;   // descriptor units
+      a[kk] = qd + off;
+      b[kk] = kd + off;
+    }
+    mma_ss_batch8(d, a, b, IDESC_S, 0u);
+  }
+  // O (+)= P V: P packed in TMEM (16 keys = 8 columns per step), V tile
+  // MN-major (16 key rows = 2048 bytes per step).
+  __device__ static void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t v_smem, bool first) {
+    const uint64_t vd = sdesc_sw128(v_smem, HALF, 1024);
+    uint32_t a[8];
+    uint64_t b[8];
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+      a[kk] = p_tmem + kk * 8;
+      b[kk] = vd + ((kk * 2048) >> 4);
+    }
+    mma_ts_batch8(d, a, b, IDESC_O, first ? 0u : 1u);
+  }
+  // four consecutive probabilities into the packed P words
+  __device__ static void pack4(uint32_t* pk, int c4, float p0, float p1, float p2, float p3) {
+    pk[2 * c4] = pack_bf16x2(p0, p1);
+    pk[2 * c4 + 1] = pack_bf16x2(p2, p3);
+  }
+};
+
+// ---- fp8 (e4m3): a 128 x 128 tile is one 128-byte swizzled box.  V is read
+// from a transposed copy V^T [d][keys], so the P V product takes both
+// operands K-major (keys contiguous), the layout every 8-bit operand shares.
+struct Fp8 : FwdLayout<BM * HD, 8> {
+  static constexpr uint32_t IDESC_S = idesc_e4m3(BM, BN);
+  static constexpr uint32_t IDESC_O = idesc_e4m3(BM, HD);
+  static constexpr int P_COLS = BN / 4;             // packed P: 4 keys per TMEM column
+
+  __device__ static void load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int row,
+                                   int head) {
+    tma_load_3d(dst, map, bar, 0, row, head);
+  }
+  // V^T tile: rows = the 128 head-dimension entries, columns = keys `key`..
+  __device__ static void load_v(uint32_t dst, const CUtensorMap* map, uint32_t bar, int key,
+                                int head) {
+    tma_load_3d(dst, map, bar, key, 0, head);
+  }
+  // S = Q K^T: 4 k-steps of 32 along d (32 bytes each), both K-major.
+  __device__ static void issue_s(uint32_t d, uint32_t q_smem, uint32_t k_smem) {
+    const uint64_t qd = sdesc_sw128(q_smem, 16, 1024);
+    const uint64_t kd = sdesc_sw128(k_smem, 16, 1024);
+    uint64_t a[4], b[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      a[kk] = qd + ((kk * 32) >> 4);
+      b[kk] = kd + ((kk * 32) >> 4);
+    }
+    mma_f8_ss_batch4(d, a, b, IDESC_S, 0u);
+  }
+  // O (+)= P V: P packed in TMEM (32 keys = 8 columns per step), V^T K-major
+  // (32 keys = 32 bytes per step).
+  __device__ static void issue_pv(uint32_t d, uint32_t p_tmem, uint32_t v_smem, bool first) {
+    const uint64_t vd = sdesc_sw128(v_smem, 16, 1024);
+    uint32_t a[4];
+    uint64_t b[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      a[kk] = p_tmem + kk * 8;
+      b[kk] = vd + ((kk * 32) >> 4);
+    }
+    mma_f8_ts_batch4(d, a, b, IDESC_O, first ? 0u : 1u);
+  }
+  __device__ static void pack4(uint32_t* pk, int c4, float p0, float p1, float p2, float p3) {
+    pk[c4] = pack_e4m3x4(p0, p1, p2, p3);
+  }
+};
+
+template <class T>
+struct Ctx {
+  uint32_t sbase;
+  volatile int* abort;
+  __device__ uint32_t bar(int i) const {
+    return sbase + T::OFF_BAR + 8u * static_cast<uint32_t>(i);
+  }
+  __device__ bool wait(int i, uint32_t parity) const {
+    return mbar_wait(bar(i), parity, abort, &g_status_fwd);
+  }
+};
+
+// The kernel body for element type T.  kWindow: a sliding window is applied
+// (window >= 1); the plain instantiation carries none of its bookkeeping.
+// out_scale multiplies O at the end (the fp8 V descale; 1 for bf16).
+template <class T, bool kWindow>
+__device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                         const CUtensorMap* tmV, __nv_bfloat16* __restrict__ O,
+                                         float* __restrict__ LSE, int BH, int N,
+                                         float scale_log2, float out_scale, int causal,
+                                         int group, int window) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::OFF_MISC + 4);
+  const Ctx<T> ctx{sbase, abort_flag};
+  constexpr int SLOTS = T::SLOTS;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int npair = (N + 2 * BM - 1) / (2 * BM);
+  const int nkv = (N + BN - 1) / BN;
+  const int pair = causal ? (npair - 1 - static_cast<int>(blockIdx.x) / BH)
+                          : (static_cast<int>(blockIdx.x) / BH);
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int bkv = bh / group;                   // key/value head of this query head
+  // key tiles [lo, nt) needed by Q block A (tile 2*pair) and B (tile 2*pair + 1)
+  const int ntA = causal ? min(2 * pair + 1, nkv) : nkv;
+  const int ntB = causal ? min(2 * pair + 2, nkv) : nkv;
+  const int loA = kWindow ? max(0, 2 * pair * BM - window + 1) / BN : 0;
+  const int loB = kWindow ? min(max(0, (2 * pair + 1) * BM - window + 1) / BN, ntB - 1) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(ctx.bar(T::B_QFULL), 1);
+    for (int s = 0; s < SLOTS; ++s) {
+      mbar_init(ctx.bar(T::B_FULL + s), 1);
+      mbar_init(ctx.bar(T::B_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(ctx.bar(T::B_SFULL + b), 1);
+      mbar_init(ctx.bar(T::B_PFULL + b), 4);
+      mbar_init(ctx.bar(T::B_ODONE + b), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == WARP_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(tmQ);
+      prefetch_tmap(tmK);
+      prefetch_tmap(tmV);
+      const uint32_t qf = ctx.bar(T::B_QFULL);
+      const int q0 = pair * 2 * BM;
+      mbar_arrive_expect_tx(qf, 2 * T::TILE);
+      T::load_rows(sbase + T::OFF_QA, tmQ, qf, q0, bh);
+      T::load_rows(sbase + T::OFF_QB, tmQ, qf, q0 + BM, bh);
+      bool ok = true;
+      int cnt = 0;
+      for (int j = loA; j < ntB && ok; ++j) {
+        for (int which = 0; which < 2 && ok; ++which, ++cnt) {
+          const int slot = cnt % SLOTS;
+          if (cnt >= SLOTS && !ctx.wait(T::B_EMPTY + slot, ((cnt / SLOTS) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ctx.bar(T::B_FULL + slot);
+          const uint32_t dst = sbase + T::OFF_SLOT + slot * T::TILE;
+          mbar_arrive_expect_tx(fb, T::TILE);
+          if (which)
+            T::load_v(dst, tmV, fb, j * BN, bkv);
+          else
+            T::load_rows(dst, tmK, fb, j * BN, bkv);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // Tiles are numbered from loA: K_j sits in slot (2t) % SLOTS and V_j in
+      // (2t+1) % SLOTS with t = j - loA; the n-th fill of a slot completes
+      // phase n of its FULL barrier.  Block A works on tiles [loA, ntA) and
+      // block B on [loB, ntB), with loB <= loA + 1 and ntB >= ntA, so B takes
+      // every tile after the first.
+      auto full_k = [&](int j) {
+        const int t = j - loA;
+        return ctx.wait(T::B_FULL + (2 * t) % SLOTS, ((2 * t) / SLOTS) & 1);
+      };
+      auto full_v = [&](int j) {
+        const int t = j - loA;
+        return ctx.wait(T::B_FULL + (2 * t + 1) % SLOTS, ((2 * t + 1) / SLOTS) & 1);
+      };
+      auto active_a = [&](int j) { return j < ntA; };
+      auto active_b = [&](int j) { return j >= loB; };
+      bool ok = ctx.wait(T::B_QFULL, 0) && full_k(loA);
+      if (ok) {
+        tc_fence_after();
+        T::issue_s(tmem + TM_S, sbase + T::OFF_QA, sbase + T::OFF_SLOT);
+        mma_commit(ctx.bar(T::B_SFULL + 0));
+        if (active_b(loA)) {
+          T::issue_s(tmem + TM_S + 128, sbase + T::OFF_QB, sbase + T::OFF_SLOT);
+          mma_commit(ctx.bar(T::B_SFULL + 1));
+        }
+        mma_commit(ctx.bar(T::B_EMPTY + 0));
+      }
+      for (int j = loA; j < ntB && ok; ++j) {
+        const int t = j - loA;
+        const int vslot = (2 * t + 1) % SLOTS;
+        const int kslot_next = (2 * t + 2) % SLOTS;
+        bool v_ready = false, k_next_ready = false;
+        if (active_a(j)) {
+          ok = ctx.wait(T::B_PFULL + 0, (j - loA) & 1) && full_v(j);
+          if (!ok) break;
+          v_ready = true;
+          tc_fence_after();
+          T::issue_pv(tmem + TM_O, tmem + TM_S, sbase + T::OFF_SLOT + vslot * T::TILE, j == loA);
+          if (j == ntA - 1) mma_commit(ctx.bar(T::B_ODONE + 0));
+        }
+        if (active_a(j + 1)) {
+          ok = full_k(j + 1);
+          if (!ok) break;
+          k_next_ready = true;
+          tc_fence_after();
+          T::issue_s(tmem + TM_S, sbase + T::OFF_QA, sbase + T::OFF_SLOT + kslot_next * T::TILE);
+          mma_commit(ctx.bar(T::B_SFULL + 0));
+        }
+        if (active_b(j)) {
+          ok = ctx.wait(T::B_PFULL + 1, (j - loB) & 1) && (v_ready || full_v(j));
+          if (!ok) break;
+          tc_fence_after();
+          T::issue_pv(tmem + TM_O + 128, tmem + TM_S + 128, sbase + T::OFF_SLOT + vslot * T::TILE, j == loB);
+          if (j == ntB - 1) mma_commit(ctx.bar(T::B_ODONE + 1));
+        }
+        mma_commit(ctx.bar(T::B_EMPTY + vslot));
+        if (j + 1 < ntB) {
+          ok = k_next_ready || full_k(j + 1);
+          if (!ok) break;
+          tc_fence_after();
+          T::issue_s(tmem + TM_S + 128, sbase + T::OFF_QB, sbase + T::OFF_SLOT + kslot_next * T::TILE);
+          mma_commit(ctx.bar(T::B_SFULL + 1));
+          mma_commit(ctx.bar(T::B_EMPTY + kslot_next));
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int blk = warp >> 2;                    // 0: block A, 1: block B
+    const int quad = warp & 3;                    // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;             // row within the Q block
+    const int qt = 2 * pair + blk;                // Q tile index (128-row units)
+    const int q_row = qt * BM + row;
+    const int nt = blk ? ntB : ntA;
+    const int lo = blk ? loB : loA;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * blk;
+    const uint32_t o_addr = tmem + lane_addr + TM_O + 128 * blk;
+    float m = -INFINITY;                          // reference max, log2 units
+    float l = 0.f;                                // running sum
+    bool ok = true;
+
+    for (int j = lo; j < nt; ++j) {
+      if (!ctx.wait(T::B_SFULL + blk, (j - lo) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BN];
+      {
+        uint32_t r[BN];
+        tmem_ld128(s_addr, r);                    // the row's 128 scores in one round trip
+#pragma unroll
+        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
+      }
+      // mask: causal diagonal tile, keys past the end of the sequence, or a
+      // tile that cuts through the window's lower edge
+      const bool diag = causal && (j == qt);
+      const bool ragged = (j == nkv - 1) && (N % BN != 0);
+      const bool wedge = kWindow && j * BN < qt * BM + BM - window;
+      if (diag || ragged || wedge) {
+        // keys visible to this row: key_lo <= key <= key_hi, tested as one
+        // unsigned compare per key
+        const int key_hi = causal ? min(q_row, N - 1) : (N - 1);
+        const int key_lo = kWindow ? q_row - window + 1 : 0;
+        const uint32_t span = static_cast<uint32_t>(key_hi - key_lo);
+        const int rel0 = j * BN - key_lo;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (static_cast<uint32_t>(rel0 + c) > span) s[c] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      mx *= scale_log2;
+      // Raise the reference max only when the new one exceeds it by more
+      // than the threshold (always on the first tile, where m = -inf).
+      float corr = 1.f;
+      if (mx > m + kRescaleThreshold) {
+        corr = fast_exp2(m - mx);                 // 0 on the first tile
+        m = mx;
+      }
+      const bool rescale_o = (j > lo) && __any_sync(0xffffffffu, corr != 1.f);
+      // A row that has seen no visible key yet (only possible with a window)
+      // keeps m = -inf; it uses 0 as the exponent reference so its masked
+      // scores give exp2(-inf) = 0, not NaN.
+      const float mref = (kWindow && m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+      uint32_t pk[T::P_COLS];
+#pragma unroll
+      for (int c = 0; c < BN / 4; ++c) {
+        const float p0 = fast_exp2(fmaf(s[4 * c], scale_log2, -mref));
+        const float p1 = fast_exp2(fmaf(s[4 * c + 1], scale_log2, -mref));
+        rs += p0 + p1;
+        const float p2 = fast_exp2(fmaf(s[4 * c + 2], scale_log2, -mref));
+        const float p3 = fast_exp2(fmaf(s[4 * c + 3], scale_log2, -mref));
+        rs += p2 + p3;
+        T::pack4(pk, c, p0, p1, p2, p3);
+      }
+      l = l * corr + rs;
+      // P (packed) over the first P_COLS columns of this block's S buffer
+#pragma unroll
+      for (int c = 0; c < T::P_COLS; c += 32)
+        tmem_st32(s_addr + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+      if (rescale_o) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+          tmem_st32(o_addr + c * 32, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctx.bar(T::B_PFULL + blk));
+    }
+
+    if (ok && ctx.wait(T::B_ODONE + blk, 0)) {
+      tc_fence_after();
+      const float inv_l = out_scale / l;
+      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_addr + c * 32, r);
+        if (q_row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * i]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+        }
+      }
+      if (LSE != nullptr && q_row < N)
+        LSE[static_cast<size_t>(bh) * N + q_row] = m * kLn2 + logf(l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// kWindow: a sliding window is applied (window >= 1).
+template <bool kWindow>
+__global__ void __launch_bounds__(NTHREADS, 1)
+fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                float* __restrict__ LSE, int BH, int N, float scale_log2, int causal,
+                int group, int window) {
+  fwd_body<Bf16, kWindow>(&tmQ, &tmK, &tmV, O, LSE, BH, N, scale_log2, 1.f, causal, group,
+                          window);
+}
+
+// Q, K e4m3 [BH, N, 128]; tmV maps the transposed copy V^T [BH, 128, keys].
+template <bool kWindow>
+__global__ void __launch_bounds__(NTHREADS, 1)
+fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmVt, __nv_bfloat16* __restrict__ O,
+               float* __restrict__ LSE, int BH, int N, float scale_log2, float v_descale,
+               int causal, int group, int window) {
+  fwd_body<Fp8, kWindow>(&tmQ, &tmK, &tmVt, O, LSE, BH, N, scale_log2, v_descale, causal, group,
+                         window);
+}
+
+// V [rows, 128] e4m3 -> V^T [128, ld] per head: 64 keys x 128 columns per
+// block through shared memory (16-byte reads and writes on both sides).
+__global__ void __launch_bounds__(256) transpose_v_kernel(const uint8_t* __restrict__ v,
+                                                          uint8_t* __restrict__ vt, int N,
+                                                          int ld) {
+  __shared__ uint8_t tile[64][HD + 16];
+  const int head = blockIdx.y;
+  const int k0 = blockIdx.x * 64;
+  const uint8_t* src = v + static_cast<size_t>(head) * N * HD;
+  uint8_t* dst = vt + static_cast<size_t>(head) * HD * ld;
+  // load: 64 rows x 8 chunks of 16 bytes
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int r = i >> 3, c = i & 7;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + r < N) x = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(k0 + r) * HD + c * 16);
+    *reinterpret_cast<uint4*>(&tile[r][c * 16]) = x;
+  }
+  __syncthreads();
+  // store: 128 rows (head-dimension entries) x 4 chunks of 16 keys
+  for (int i = threadIdx.x; i < HD * 4; i += blockDim.x) {
+    const int dcol = i >> 2, c = i & 3;
+    const int key = k0 + c * 16;
+    if (key >= ld) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = static_cast<uint32_t>(tile[c * 16 + 4 * q][dcol]) |
+             (static_cast<uint32_t>(tile[c * 16 + 4 * q + 1][dcol]) << 8) |
+             (static_cast<uint32_t>(tile[c * 16 + 4 * q + 2][dcol]) << 16) |
+             (static_cast<uint32_t>(tile[c * 16 + 4 * q + 3][dcol]) << 24);
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(dcol) * ld + key) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <class K>
+cudaError_t set_smem(K kernel, uint32_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bytes));
+}
+
+}  // namespace
+
+cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
+                                int Hkv, int N, float scale, int causal, int window,
+                                cudaStream_t stream, const TimingEvents& ev) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = set_smem(fwd_bf16_kernel<false>, Bf16::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<true>, Bf16::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int BH = B * H;
+  const int npair = (N + 2 * BM - 1) / (2 * BM);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  auto kernel = window > 0 ? fwd_bf16_kernel<true> : fwd_bf16_kernel<false>;
+  if (ev.before) cudaEventRecord(ev.before, stream);
+  kernel<<<dim3(npair * BH), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
+      maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal,
+      H / Hkv, window);
+  cudaError_t e = cudaGetLastError();
+  if (ev.after) cudaEventRecord(ev.after, stream);
+  return e;
+}
+
+size_t fp8_vt_ld(int N) { return (static_cast<size_t>(N) + 15) / 16 * 16; }
+
+size_t forward_fp8_workspace_bytes(int B, int Hkv, int N) {
+  return align256(static_cast<size_t>(B) * Hkv * HD * fp8_vt_ld(N));
+}
+
+cudaError_t launch_transpose_v_fp8(const void* v, void* vt, int B, int Hkv, int N,
+                                   cudaStream_t stream) {
+  const int ld = static_cast<int>(fp8_vt_ld(N));
+  transpose_v_kernel<<<dim3((N + 63) / 64, B * Hkv), dim3(256), 0, stream>>>(
+      static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, ld);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, int H, int Hkv,
+                               int N, float scale, float q_descale, float k_descale,
+                               float v_descale, int causal, int window, cudaStream_t stream,
+                               const TimingEvents& ev) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = set_smem(fwd_fp8_kernel<false>, Fp8::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<true>, Fp8::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int BH = B * H;
+  const int npair = (N + 2 * BM - 1) / (2 * BM);
+  const float scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
+  auto kernel = window > 0 ? fwd_fp8_kernel<true> : fwd_fp8_kernel<false>;
+  if (ev.before) cudaEventRecord(ev.before, stream);
+  kernel<<<dim3(npair * BH), dim3(NTHREADS), Fp8::SMEM_BYTES, stream>>>(
+      maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, v_descale,
+      causal, H / Hkv, window);
+  cudaError_t e = cudaGetLastError();
+  if (ev.after) cudaEventRecord(ev.after, stream);
+  return e;
+}
+
+int status_forward_bf16(bool clear) {
+  int s = 0;
+  cudaMemcpyFromSymbol(&s, g_status_fwd, sizeof(int));
+  if (clear && s != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_status_fwd, &zero, sizeof(int));
+  }
+  return s;
+}
+
+}  // namespace fa

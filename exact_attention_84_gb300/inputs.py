@@ -52,8 +52,13 @@ WINDOW_N8192 = Workload("bf16 causal sliding-window (w=1024) forward B1 H32 N819
                         8192, 128, torch.bfloat16, 6, causal=True, window=1024)
 GQA_DECODE_L32K = Workload("bf16 GQA split-KV decode B64 Hq32 Hkv8 Lkv32768 d128", 64, 32,
                            32768, 128, torch.bfloat16, 7, kind="decode", Hkv=8)
+# FP8 (E4M3) inputs: N(0,1) draws times FP8_AMP, rounded to E4M3; descale
+# factor 1/FP8_AMP for each tensor.
+FP8_LONG_CAUSAL = Workload("fp8 e4m3 causal forward B1 H32 N8192 d128", 1, 32, 8192, 128,
+                           torch.float8_e4m3fn, 8, causal=True)
+FP8_AMP = 16.0
 ALL = [TINY_FP32, FWD_N2048, LONG_CAUSAL, TRAIN_N4096, DECODE_L32K, GQA_TRAIN_N4096,
-       WINDOW_N8192, GQA_DECODE_L32K]
+       WINDOW_N8192, GQA_DECODE_L32K, FP8_LONG_CAUSAL]
 
 
 def _draw(g, shape_per_batch, B, dtype, device):
@@ -95,6 +100,21 @@ def gqa_inputs(B, Hq, Hkv, N, d, dtype, seed, device, with_do=False):
     return q, k, v
 
 
+def fp8_inputs(B, Hq, Hkv, N, d, seed, device, amp=FP8_AMP):
+    """E4M3 codes as uint8: q [B, Hq, N, d], k, v [B, Hkv, N, d], each drawn
+    as fp32 N(0,1) times `amp` and rounded to E4M3 (values stay far below
+    the format's 448 limit)."""
+    g = generator(seed, device)
+    out = []
+    for h in (Hq, Hkv, Hkv):
+        t = torch.empty((B, h, N, d), dtype=torch.uint8, device=device)
+        for b in range(B):
+            x = torch.randn((h, N, d), generator=g, device=device, dtype=torch.float32) * amp
+            t[b] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        out.append(t)
+    return tuple(out)
+
+
 def decode_gqa_inputs(B, Hq, Hkv, L, d, dtype, seed, device):
     """q [B, Hq, d] and contiguous caches [B, Hkv, L, d]."""
     g = generator(seed, device)
@@ -114,6 +134,8 @@ def decode_inputs(B, H, L, d, dtype, seed, device):
 
 
 def workload_inputs(w: Workload, device):
+    if w.dtype == torch.float8_e4m3fn:
+        return fp8_inputs(w.B, w.H, w.kv_heads, w.N, w.d, w.seed, device)
     if w.Hkv is not None:
         if w.kind == "decode":
             return decode_gqa_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.dtype, w.seed, device)

@@ -59,7 +59,7 @@ typedef enum {
 } fa_status;
 
 /* Operation codes for fa_workspace_size(). */
-enum { FA_OP_FORWARD = 0, FA_OP_BACKWARD = 1, FA_OP_DECODE = 2 };
+enum { FA_OP_FORWARD = 0, FA_OP_BACKWARD = 1, FA_OP_DECODE = 2, FA_OP_FORWARD_FP8 = 3 };
 
 /*
  * fa_forward -- fused tiled forward pass, bf16 in / bf16 out.
@@ -118,6 +118,32 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o,
 int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                    int window, cudaStream_t stream);
+
+/*
+ * fa_forward_fp8 -- the forward pass with 8-bit floating-point inputs
+ * ("03. FlashAttention", "FlashAttention v3": hardware FP8 as a lever).
+ *
+ * q, k, v hold OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinities; 0x7F/0xFF are NaN), one byte per element,
+ * in the layouts of fa_forward_gqa.  Their real values are code * descale:
+ *   O = softmax(scale * (q_descale Q)(k_descale K)^T [+ mask]) (v_descale V)
+ * Products run on the tensor cores with fp32 accumulation; P is rounded to
+ * E4M3 (round to nearest even) before the P V product, which adds an error
+ * of at most 2^-4 relative to each weight.  o is bf16, lse fp32 (natural
+ * log), as in fa_forward.
+ *
+ *   Hkv, causal, window  as in fa_forward_gqa.
+ *   descale factors      finite and > 0.
+ *   ws                   NULL: a workspace (a transposed copy of V) comes
+ *                        from the library pool; otherwise a caller buffer of
+ *                        ws_bytes >= fa_workspace_size(FA_OP_FORWARD_FP8,
+ *                        B, Hkv, N, d, 0) bytes, 256-byte aligned.
+ *   d must be 128.  Returns as fa_forward, or FA_ERR_NO_MEMORY.
+ */
+int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int Hq, int Hkv, int N, int d, float scale, float q_descale,
+                   float k_descale, float v_descale, int causal, int window, void* ws,
+                   size_t ws_bytes, cudaStream_t stream);
 
 /*
  * fa_backward -- gradients dQ, dK, dV by recomputation.
@@ -252,8 +278,10 @@ int fa_decode_noalloc(const void* q, const void* kcache, const void* vcache,
 
 /*
  * fa_workspace_size -- device workspace bytes needed by an operation.
- *   op           FA_OP_FORWARD (always 0), FA_OP_BACKWARD or FA_OP_DECODE.
- *   H            the number of query heads (Hq for the _gqa calls).
+ *   op           FA_OP_FORWARD (always 0), FA_OP_BACKWARD, FA_OP_DECODE or
+ *                FA_OP_FORWARD_FP8.
+ *   H            the number of query heads (Hq for the _gqa calls); for
+ *                FA_OP_FORWARD_FP8 the number of key/value heads Hkv.
  *   n_or_lkv     N for forward/backward, Lkv for decode.
  *   num_splits   decode only; ignored otherwise.
  * Returns 0 for invalid arguments.

@@ -15,3 +15,4 @@ from .attention import (  # noqa: F401
     online_softmax_stats,
     tiled_attention_row,
 )
+from .fp8 import attention_forward_fp8, decode_e4m3  # noqa: F401
