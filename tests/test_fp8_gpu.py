@@ -14,8 +14,21 @@ with P, V the exact (oracle) weights and decoded values, sum_j over the keys
 row i sees, and l_i = sum_j exp(s_ij - max_j s_ij) >= 1 (the kernel's l is
 taken relative to a reference no larger than the row maximum, so it is at
 least this large).  The last terms cover the bf16 output rounding and fp32
-accumulation.  The mean error must stay within the bf16 path's 2e-3 and LSE
-within 1e-3 (l uses unrounded weights).
+accumulation.
+
+Mean error: rounding to 3 mantissa bits leaves each weight an error spread
+over at most one unit in the last place, 2^-3 p_j (2^-9 / l_i in normalised
+units below 2^-6), so its standard deviation is at most that over sqrt(12)
+and, summed over the keys,
+
+  sigma_ic = v_descale * sqrt(2^-6/12 sum_j P_ij^2 V_jc^2
+                              + 2^-18/12 sum_j V_jc^2 / l_i^2).
+
+The mean of |dO| over all elements (about 0.8 sigma for independent
+roundings) must not exceed the mean of sigma plus the bf16 output rounding
+(2^-9 |O| on average at most).  The bf16 path's 2e-3 does not carry over:
+its P keeps 8 mantissa bits.  LSE stays within 1e-3 (l uses unrounded
+weights).
 """
 import math
 
@@ -26,7 +39,7 @@ import torch
 import oracle.attention as orc
 import oracle.fp8 as f8
 from exact_attention_84_gb300 import _lib, api, inputs
-from gpu_common import LSE_MAX, O_MEAN, guarded, guards_intact, np64, status_clean  # noqa: F401
+from gpu_common import LSE_MAX, guarded, guards_intact, np64, status_clean  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -36,9 +49,9 @@ DS = 1 / inputs.FP8_AMP
 
 
 def fp8_bound(qd, kd, vd, o_ref, scale, causal, window, v_descale, rows=None):
-    """Per-element error bound above, for one head: qd [R, d] the query rows
-    at positions `rows` (default: all), kd [N, d] decoded and descaled, vd
-    [N, d] decoded (v_descale applied here), o_ref [R, d]."""
+    """Per-element error bound and sigma above, for one head: qd [R, d] the
+    query rows at positions `rows` (default: all), kd [N, d] decoded and
+    descaled, vd [N, d] decoded (v_descale applied here), o_ref [R, d]."""
     rows = np.arange(qd.shape[0]) if rows is None else np.asarray(rows)
     s = (qd @ kd.T) * scale
     i = rows[:, None]
@@ -54,8 +67,12 @@ def fp8_bound(qd, kd, vd, o_ref, scale, causal, window, v_descale, rows=None):
     l = w.sum(axis=1, keepdims=True)
     p = w / l
     av = np.abs(vd)
-    return (v_descale * (2.0 ** -4 * (p @ av) + 2.0 ** -10 * (vis @ av) / l)
-            + 2.0 ** -8 * np.abs(o_ref) + 1e-4)
+    bound = (v_descale * (2.0 ** -4 * (p @ av) + 2.0 ** -10 * (vis @ av) / l)
+             + 2.0 ** -8 * np.abs(o_ref) + 1e-4)
+    v2 = vd * vd
+    sigma = v_descale * np.sqrt(2.0 ** -6 / 12 * ((p * p) @ v2)
+                                + 2.0 ** -18 / 12 * (vis @ v2) / (l * l))
+    return bound, sigma
 
 
 def check_fp8(o, lse, q8, k8, v8, scale, causal, window, descales, what):
@@ -67,19 +84,22 @@ def check_fp8(o, lse, q8, k8, v8, scale, causal, window, descales, what):
     err = np.abs(got - o_ref)
     g = q8.shape[1] // k8.shape[1]
     worst = 0.0
+    sig = np.zeros_like(err)
     for b in range(q8.shape[0]):
         for h in range(q8.shape[1]):
             qd = f8.decode_e4m3(q8n[b, h]) * qs
             kd = f8.decode_e4m3(k8n[b, h // g]) * ks
             vd = f8.decode_e4m3(v8n[b, h // g])
-            bound = fp8_bound(qd, kd, vd, o_ref[b, h], scale, causal, window, vs)
+            bound, sig[b, h] = fp8_bound(qd, kd, vd, o_ref[b, h], scale, causal, window, vs)
             ratio = (err[b, h] / bound).max()
             worst = max(worst, ratio)
             assert ratio <= 1.0, f"{what} ({b},{h}): error exceeds the bound by x{ratio:.2f}"
-    assert err.mean() <= O_MEAN, f"{what} mean|dO| = {err.mean():.3e}"
+    mean_lim = sig.mean() + 2.0 ** -9 * np.abs(o_ref).mean() + 1e-5
+    assert err.mean() <= mean_lim, f"{what} mean|dO| = {err.mean():.3e} > {mean_lim:.3e}"
     dl = np.abs(np64(lse) - lse_ref).max()
     assert dl <= LSE_MAX, f"{what} max|dLSE| = {dl:.3e}"
-    print(f"{what}: max|dO| {err.max():.3e} mean {err.mean():.3e} worst/bound {worst:.3f}")
+    print(f"{what}: max|dO| {err.max():.3e} mean {err.mean():.3e} (limit {mean_lim:.3e}) "
+          f"worst/bound {worst:.3f}")
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 1, 1, 1), (1, 2, 2, 128), (2, 2, 1, 300),
@@ -132,7 +152,7 @@ def test_fp8_long_causal_n8192_sampled():
         o_ref, lse_ref = orc.attention_forward_rows(qd[rows], kd, vd * DS, rows, SCALE, True)
         got = np64(o[0, h, rows])
         err = np.abs(got - o_ref)
-        bound = fp8_bound(qd[rows], kd, vd, o_ref, SCALE, True, 0, DS, rows=rows)
+        bound, sig = fp8_bound(qd[rows], kd, vd, o_ref, SCALE, True, 0, DS, rows=rows)
         assert (err <= bound).all(), f"head {h}: x{(err / bound).max():.2f} over the bound"
-        assert err.mean() <= O_MEAN
+        assert err.mean() <= sig.mean() + 2.0 ** -9 * np.abs(o_ref).mean() + 1e-5
         assert np.abs(np64(lse[0, h, rows]) - lse_ref).max() <= LSE_MAX
