@@ -21,8 +21,9 @@ The same line carries:
                 in KV GB/s against the measured HBM copy bandwidth; then the
                 grouped-query forward and backward kernels (B8 Hq32 Hkv8
                 N4096 causal), the causal sliding-window forward (w = 1024,
-                B1 H32 N8192) and grouped-query decode (B64 Hq32 Hkv8
-                Lkv32768);
+                B1 H32 N8192), grouped-query decode (B64 Hq32 Hkv8
+                Lkv32768) and the fp8 (E4M3) causal forward B1 H32 N8192
+                against the fp8 dense peak;
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload;
   clocks        SM clocks and throttle reasons sampled during the timed loop.
 
@@ -499,6 +500,40 @@ def measure_targets(args, dev, peaks, peak_src):
         "peak_kind": f"bf16 dense, burst ({peak_src})", "l2_flush": False,
         "flops": "4 d per visible (query, key) pair"}
     del q, k, v, o, lse
+
+    # FP8 (E4M3) causal forward: the main kernel against the fp8 dense peak
+    # (the measured bf16 peak times the nominal fp8/bf16 ratio 4.5/2.25), and
+    # the whole call (V transposition included)
+    w = inputs.FP8_LONG_CAUSAL
+    q8, k8, v8 = inputs.workload_inputs(w, dev)
+    o = torch.empty(q8.shape, device=dev, dtype=torch.bfloat16)
+    lse = torch.empty(q8.shape[:3], device=dev, dtype=torch.float32)
+    ws = torch.empty(_lib.fa_workspace_size(_lib.FA_OP_FORWARD_FP8, w.B, w.H, w.N, w.d, 0),
+                     dtype=torch.uint8, device=dev)
+    ds = 1.0 / inputs.FP8_AMP
+    call = lambda: _lib.check(_lib.fa_forward_fp8(  # noqa: E731
+        q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H,
+        w.H, w.N, w.d, 1 / math.sqrt(w.d), ds, ds, ds, 1, 0, ws.data_ptr(), ws.numel(), sh))
+    ms = time_kernel(call, False)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a, b = lib_event(), lib_event()
+    a.record()
+    for _ in range(iters):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms_call = a.elapsed_time(b) / iters
+    fl = acc.forward_flops(w.B, w.H, w.N, w.d, True)
+    fp8_peak = 2.0 * burst
+    t = fl / (ms * 1e-3) / 1e12
+    out["forward_fp8_causal_B1_H32_N8192"] = {
+        "ms": round(ms, 4), "tflops": round(t, 1), "frac": round(t / fp8_peak, 4),
+        "peak": fp8_peak, "peak_kind": f"fp8 dense = 2 x bf16 burst ({peak_src}), nominal ratio",
+        "call_ms": round(ms_call, 4),
+        "call_tflops": round(fl / (ms_call * 1e-3) / 1e12, 1), "l2_flush": False}
+    del q8, k8, v8, o, lse, ws
 
     # grouped-query decode: the cache (Hkv heads) read once for all query heads
     w = inputs.GQA_DECODE_L32K
