@@ -65,7 +65,7 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def _head_forward(q, k, v, scale, causal, rows, window=None):
+def _head_forward(q, k, v, scale, causal, rows, window=None, slope=None):
     """One head: q [Nq, d] (the query rows listed in ``rows``), k/v [Nk, d].
 
     Step 1 of "Le probleme": S = Q.K^T (times scale, "FlashAttention
@@ -74,6 +74,10 @@ def _head_forward(q, k, v, scale, causal, rows, window=None):
     subtracting the maximum keeps the exponents small).  Step 3: O = P.V.
     """
     s = (q @ k.T) * scale                      # [Nq, Nk]
+    if slope is not None:
+        # ALiBi: linear bias -slope * |i - j| on the scaled score
+        dist = np.abs(np.asarray(rows)[:, None] - np.arange(k.shape[0])[None, :])
+        s = s - slope * dist
     if causal:
         cols = np.arange(k.shape[0])[None, :]
         s = np.where(cols > np.asarray(rows)[:, None], -np.inf, s)
@@ -107,17 +111,19 @@ def attention_forward(q, k, v, scale: float, causal: bool):
     return o, lse
 
 
-def attention_forward_rows(q_rows, k, v, rows, scale: float, causal: bool, window=None):
+def attention_forward_rows(q_rows, k, v, rows, scale: float, causal: bool, window=None,
+                           slope=None):
     """The same definition for a chosen subset of query rows of ONE head.
 
     ``q_rows`` [R, d] are the query vectors at positions ``rows`` (needed for
     the causal mask); ``k``, ``v`` [N, d] are the head's full key/value
     matrices.  Each output row depends only on its own query row, so this is
     the definition evaluated row by row, not a blocking of it.  ``window``
-    (optional) applies the sliding-window mask described further down.
+    and ``slope`` (optional) apply the sliding-window mask and the ALiBi
+    bias described further down.
     """
     o, lse, _ = _head_forward(_f64(q_rows), _f64(k), _f64(v), scale, causal,
-                              np.asarray(rows), window)
+                              np.asarray(rows), window, slope)
     return o, lse
 
 
@@ -222,12 +228,20 @@ def tiled_attention_row(q, k, v, scale: float, tile: int):
 # h // (Hq / Hkv).  Sliding window ("03. FlashAttention", "Variantes et
 # extensions": only the K_j inside the window are considered): query i sees
 # keys i - window + 1 .. i (used together with the causal mask).
+# ALiBi ("03. FlashAttention", "Variantes et extensions": the linear bias
+# integrated into the kernel): head h adds -slope_h * |i - j| to the scaled
+# score S_ij = scale q_i.k_j before the softmax (under the causal mask this
+# is slope_h * (j - i)); slopes are given per query head.
 # --------------------------------------------------------------------------
 def _kv_head(h, hq, hkv):
     return h // (hq // hkv)
 
 
-def attention_forward_gqa(q, k, v, scale: float, causal: bool, window=None):
+def _slope(alibi_slopes, h):
+    return None if alibi_slopes is None else float(alibi_slopes[h])
+
+
+def attention_forward_gqa(q, k, v, scale: float, causal: bool, window=None, alibi_slopes=None):
     """q [B, Hq, N, d], k/v [B, Hkv, N, d] -> (O [B, Hq, N, d], LSE [B, Hq, N])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, hq, n, _ = q.shape
@@ -239,11 +253,12 @@ def attention_forward_gqa(q, k, v, scale: float, causal: bool, window=None):
         for h in range(hq):
             g = _kv_head(h, hq, hkv)
             o[b, h], lse[b, h], _ = _head_forward(q[b, h], k[b, g], v[b, g], scale, causal, rows,
-                                                  window)
+                                                  window, _slope(alibi_slopes, h))
     return o, lse
 
 
-def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None):
+def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None,
+                           alibi_slopes=None):
     """Gradients for grouped heads: dQ per query head; dK, dV of a key/value
     head are the sums over the query heads that read it."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -256,7 +271,8 @@ def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None)
     for b in range(B):
         for h in range(hq):
             g = _kv_head(h, hq, hkv)
-            o, _, p = _head_forward(q[b, h], k[b, g], v[b, g], scale, causal, rows, window)
+            o, _, p = _head_forward(q[b, h], k[b, g], v[b, g], scale, causal, rows, window,
+                                    _slope(alibi_slopes, h))
             gr = do[b, h]
             dv[b, g] += p.T @ gr                  # dV summed over the group
             dpg = gr @ v[b, g].T
@@ -267,8 +283,10 @@ def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None)
     return dq, dk, dv
 
 
-def attention_decode_gqa(q, kcache, vcache, scale: float):
-    """q [B, Hq, d], caches [B, Hkv, L, d] -> (o [B, Hq, d], lse [B, Hq])."""
+def attention_decode_gqa(q, kcache, vcache, scale: float, alibi_slopes=None):
+    """q [B, Hq, d], caches [B, Hkv, L, d] -> (o [B, Hq, d], lse [B, Hq]).
+    The new query sits at position L - 1, after every cached row (ALiBi
+    distance L - 1 - j)."""
     q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
     B, hq, _ = q.shape
     hkv = kc.shape[1]
@@ -278,6 +296,8 @@ def attention_decode_gqa(q, kcache, vcache, scale: float):
         for h in range(hq):
             g = _kv_head(h, hq, hkv)
             s = (kc[b, g] @ q[b, h]) * scale
+            if alibi_slopes is not None:
+                s = s - float(alibi_slopes[h]) * (s.shape[0] - 1 - np.arange(s.shape[0]))
             m = s.max()
             e = np.exp(s - m)
             l = e.sum()

@@ -427,6 +427,79 @@ def pin_gqa_window_torch(orc):
     assert np.abs(od - ref[:, :, 0].numpy()).max() < 1e-12
 
 
+def pin_alibi_closed_forms(orc):
+    """ALiBi: identical keys leave only the bias, so causal row i weights key
+    j by e^(-m (i - j)), a geometric series with a closed-form sum; slope 0
+    is plain attention; a steep slope leaves only the diagonal."""
+    r = _rng(61)
+    n, d = 9, 4
+    q, v = (r.standard_normal((1, 2, n, d)) for _ in range(2))
+    k = np.repeat(r.standard_normal((1, 1, 1, d)), n, axis=2).repeat(2, axis=1)
+    slopes = np.array([0.5, 0.125])
+    o, lse = orc.attention_forward_gqa(q, k, v, 0.7, True, alibi_slopes=slopes)
+    for h in range(2):
+        m = slopes[h]
+        for i in range(n):
+            w = np.exp(-m * (i - np.arange(i + 1)))
+            want = (w[:, None] * v[0, h, :i + 1]).sum(axis=0) / w.sum()
+            assert np.abs(o[0, h, i] - want).max() < 1e-14
+            series = (1 - math.exp(-m * (i + 1))) / (1 - math.exp(-m))
+            assert abs(lse[0, h, i] - (0.7 * q[0, h, i] @ k[0, h, 0] + math.log(series))) < 1e-13
+    # non-causal: the bias is symmetric in |i - j|
+    o_nc, _ = orc.attention_forward_gqa(q, k, v, 0.7, False, alibi_slopes=slopes)
+    for h in range(2):
+        w = np.exp(-slopes[h] * np.abs(3 - np.arange(n)))
+        want = (w[:, None] * v[0, h]).sum(axis=0) / w.sum()
+        assert np.abs(o_nc[0, h, 3] - want).max() < 1e-14
+    q2, k2, v2 = (r.standard_normal((1, 2, n, d)) for _ in range(3))
+    o0, l0 = orc.attention_forward_gqa(q2, k2, v2, 0.5, True, alibi_slopes=np.zeros(2))
+    ob, lb = orc.attention_forward(q2, k2, v2, 0.5, True)
+    assert np.abs(o0 - ob).max() < 1e-15 and np.abs(l0 - lb).max() < 1e-15
+    os_, ls = orc.attention_forward_gqa(q2, k2, v2, 0.5, False, alibi_slopes=np.full(2, 2000.0))
+    assert np.abs(os_ - v2).max() < 1e-15
+    assert np.abs(ls - 0.5 * (q2 * k2).sum(-1)).max() < 1e-12
+    # decode: the new token is at position L - 1
+    od, ld = orc.attention_decode_gqa(q2[:, :, -1], k2, v2, 0.5, alibi_slopes=slopes)
+    of, lf = orc.attention_forward_gqa(q2, k2, v2, 0.5, True, alibi_slopes=slopes)
+    assert np.abs(od - of[:, :, -1]).max() < 1e-14 and np.abs(ld - lf[:, :, -1]).max() < 1e-14
+
+
+def pin_alibi_torch(orc):
+    """Library special case: PyTorch's fp64 attention with the bias given as
+    a float mask (-inf where causal hides a key), and its autograd gradients;
+    grouped heads and a window on top."""
+    import torch
+    import torch.nn.functional as F
+
+    g = torch.Generator().manual_seed(9)
+    b, hq, hkv, n, d = 2, 4, 2, 29, 8
+    q, do = (torch.randn(b, hq, n, d, generator=g, dtype=torch.float64) for _ in range(2))
+    k, v = (torch.randn(b, hkv, n, d, generator=g, dtype=torch.float64) for _ in range(2))
+    slopes = torch.tensor([0.5, 0.25, 0.125, 0.0625], dtype=torch.float64)
+    idx = torch.arange(n)
+    dist = (idx[:, None] - idx[None, :]).abs().to(torch.float64)
+    for causal, window in ((False, None), (True, None), (True, 7)):
+        bias = -slopes[:, None, None] * dist
+        if causal:
+            bias = bias.masked_fill(idx[None, :] > idx[:, None], float("-inf"))
+        if window:
+            bias = bias.masked_fill(idx[None, :] <= idx[:, None] - window, float("-inf"))
+        qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+        ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=bias, scale=0.3,
+                                             enable_gqa=True)
+        ref.backward(do)
+        o, lse = orc.attention_forward_gqa(q.numpy(), k.numpy(), v.numpy(), 0.3, causal, window,
+                                           slopes.numpy())
+        assert np.abs(o - ref.detach().numpy()).max() < 1e-12
+        s = (q @ k.repeat_interleave(hq // hkv, dim=1).transpose(-1, -2)) * 0.3 + bias
+        assert np.abs(lse - torch.logsumexp(s, dim=-1).numpy()).max() < 1e-12
+        dq, dk, dv = orc.attention_backward_gqa(q.numpy(), k.numpy(), v.numpy(), do.numpy(),
+                                                0.3, causal, window, slopes.numpy())
+        assert np.abs(dq - qq.grad.numpy()).max() < 1e-12
+        assert np.abs(dk - kk.grad.numpy()).max() < 1e-12
+        assert np.abs(dv - vv.grad.numpy()).max() < 1e-12
+
+
 ALL_PINS = [
     pin_walkthrough_softmax,
     pin_walkthrough_online,
@@ -442,4 +515,6 @@ ALL_PINS = [
     pin_gqa_repeat_kv,
     pin_window_closed_forms,
     pin_gqa_window_torch,
+    pin_alibi_closed_forms,
+    pin_alibi_torch,
 ]

@@ -40,6 +40,13 @@ MUTANTS = {
     "window_one_too_wide": ("np.asarray(rows)[:, None] - window + 1", "np.asarray(rows)[:, None] - window"),
     "window_one_too_narrow": ("np.asarray(rows)[:, None] - window + 1",
                               "np.asarray(rows)[:, None] - window + 2"),
+    "alibi_sign": ("s = s - slope * dist", "s = s + slope * dist"),
+    "alibi_scaled_twice": ("s = s - slope * dist", "s = s - slope * scale * dist"),
+    "alibi_signed_distance": ("dist = np.abs(np.asarray(rows)[:, None] - np.arange(k.shape[0])[None, :])",
+                              "dist = np.asarray(rows)[:, None] - np.arange(k.shape[0])[None, :]"),
+    "alibi_next_head": ("return None if alibi_slopes is None else float(alibi_slopes[h])",
+                        "return None if alibi_slopes is None else float(alibi_slopes[(h + 1) % len(alibi_slopes)])"),
+    "alibi_decode_position": ("(s.shape[0] - 1 - np.arange(s.shape[0]))", "(s.shape[0] - np.arange(s.shape[0]))"),
     "tiled_no_out_rescale": ("o = corr * o + p @ v[start:start + tile]",
                              "o = o + p @ v[start:start + tile]"),
 }
