@@ -470,11 +470,11 @@ def measure_targets(args, dev, peaks, peak_src):
                      dtype=torch.uint8, device=dev)
     fwd = lambda: _lib.check(_lib.fa_forward_gqa(  # noqa: E731
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, hkv,
-        w.N, w.d, scale, 1, 0, sh))
+        w.N, w.d, scale, 1, 0, None, sh))
     bwd = lambda: _lib.check(_lib.fa_backward_gqa(  # noqa: E731
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, hkv, w.N, w.d, scale, 1, 0,
-        ws.data_ptr(), ws.numel(), sh))
+        None, ws.data_ptr(), ws.numel(), sh))
     fl = acc.forward_flops(w.B, w.H, w.N, w.d, True)
     for key, call, flops in (("forward_gqa_causal_B8_Hq32_Hkv8_N4096", fwd, fl),
                              ("backward_gqa_causal_B8_Hq32_Hkv8_N4096", bwd, 2.5 * fl)):
@@ -492,7 +492,7 @@ def measure_targets(args, dev, peaks, peak_src):
     lse = torch.empty(q.shape[:3], device=dev, dtype=torch.float32)
     ms = time_kernel(lambda: _lib.check(_lib.fa_forward_gqa(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.H,
-        w.N, w.d, 1 / math.sqrt(w.d), 1, w.window, sh)), False)
+        w.N, w.d, 1 / math.sqrt(w.d), 1, w.window, None, sh)), False)
     fl = acc.masked_forward_flops(w.B, w.H, w.N, w.d, True, w.window)
     t = fl / (ms * 1e-3) / 1e12
     out["forward_window1024_B1_H32_N8192"] = {
@@ -513,7 +513,8 @@ def measure_targets(args, dev, peaks, peak_src):
     ds = 1.0 / inputs.FP8_AMP
     call = lambda: _lib.check(_lib.fa_forward_fp8(  # noqa: E731
         q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H,
-        w.H, w.N, w.d, 1 / math.sqrt(w.d), ds, ds, ds, 1, 0, ws.data_ptr(), ws.numel(), sh))
+        w.H, w.N, w.d, 1 / math.sqrt(w.d), ds, ds, ds, 1, 0, None, ws.data_ptr(), ws.numel(),
+        sh))
     ms = time_kernel(call, False)
     for _ in range(3):
         call()

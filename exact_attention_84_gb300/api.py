@@ -24,13 +24,23 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
+def _slopes(alibi_slopes, heads):
+    if alibi_slopes is None:
+        return None
+    _need(alibi_slopes, torch.float32, "alibi_slopes")
+    if alibi_slopes.numel() != heads:
+        raise ValueError(f"alibi_slopes needs {heads} entries")
+    return alibi_slopes.data_ptr()
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            window: int = 0):
+            window: int = 0, alibi_slopes=None):
     """O, LSE = attention(q, k, v) for [B, H, N, d] bf16 (or fp32) tensors.
 
     bf16 only: k and v may have fewer heads Hkv (H a multiple of Hkv; query
-    head h reads key/value head h // (H // Hkv)), and ``window`` w >= 1 (with
-    ``causal``) lets query i see keys i-w+1 .. i only."""
+    head h reads key/value head h // (H // Hkv)), ``window`` w >= 1 (with
+    ``causal``) lets query i see keys i-w+1 .. i only, and ``alibi_slopes``
+    (a CUDA fp32 tensor of H slopes) adds -slope_h * |i - j| to the scores."""
     B, H, N, d = q.shape
     Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -41,11 +51,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     o = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
-    if Hkv != H or window:
+    if Hkv != H or window or alibi_slopes is not None:
         if fp32:
-            raise ValueError("grouped heads and windows need bf16 tensors")
+            raise ValueError("grouped heads, windows and ALiBi need bf16 tensors")
         _lib.check(_lib.fa_forward_gqa(*ptrs, B, H, Hkv, N, d, scale, int(causal), int(window),
-                                       _stream()))
+                                       _slopes(alibi_slopes, H), _stream()))
     else:
         fn = _lib.fa_forward_fp32 if fp32 else _lib.fa_forward
         _lib.check(fn(*ptrs, B, H, N, d, scale, int(causal), _stream()))
@@ -54,7 +64,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 def forward_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float,
                 causal: bool = False, scale: float | None = None, window: int = 0, out=None,
-                lse=None, workspace=None):
+                lse=None, workspace=None, alibi_slopes=None):
     """O (bf16), LSE for E4M3 inputs held as uint8 codes: q8 [B, H, N, d],
     k8, v8 [B, Hkv, N, d]; real values are code * descale."""
     B, H, N, d = q8.shape
@@ -68,13 +78,13 @@ def forward_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _lib.check(_lib.fa_forward_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(),
                                    lse.data_ptr(), B, H, Hkv, N, d, scale, q_descale, k_descale,
-                                   v_descale, int(causal), int(window), ws_ptr, ws_bytes,
-                                   _stream()))
+                                   v_descale, int(causal), int(window),
+                                   _slopes(alibi_slopes, H), ws_ptr, ws_bytes, _stream()))
     return o, lse
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-             workspace=None, out=None, window: int = 0):
+             workspace=None, out=None, window: int = 0, alibi_slopes=None):
     """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``.
     ``out`` may hold three preallocated tensors (dq, dk, dv) to write into.
     k, v (and dk, dv) may have fewer heads, and ``window`` applies, as in
@@ -94,11 +104,12 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
     args = ptrs + (B, H, N, d, scale, int(causal))
-    if Hkv != H or window:
+    if Hkv != H or window or alibi_slopes is not None:
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
         _lib.check(_lib.fa_backward_gqa(*ptrs, B, H, Hkv, N, d, scale, int(causal), int(window),
-                                        ws_ptr, ws_bytes, _stream()))
+                                        _slopes(alibi_slopes, H), ws_ptr, ws_bytes,
+                                        _stream()))
     elif workspace is None:
         _lib.check(_lib.fa_backward(*args, _stream()))
     else:

@@ -168,40 +168,43 @@ extern "C" {
 
 static int forward_impl(const char* fn, const void* q, const void* k, const void* v, void* o,
                         float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
-                        int causal, int window, cudaStream_t stream) {
+                        int causal, int window, const float* alibi, cudaStream_t stream) {
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (int r = check_sizes(B, Hq, N, d)) return r;
   if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
   if (int r = check_scale(scale)) return r;
   if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (alibi && (reinterpret_cast<uintptr_t>(alibi) & 3u)))
     return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
   fa::FwdMaps maps;
   if (int r = make_map(&maps.q, q, B * Hq, N, 128)) return r;
   if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
   return launch_result(fa::launch_forward_bf16(maps, o, lse, B, Hq, Hkv, N, scale, causal,
-                                               window >= N ? 0 : window, stream, g_events),
+                                               window >= N ? 0 : window, alibi, stream,
+                                               g_events),
                        "forward launch");
 }
 
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int N, int d, float scale, int causal, cudaStream_t stream) {
-  return forward_impl("fa_forward", q, k, v, o, lse, B, H, H, N, d, scale, causal, 0, stream);
+  return forward_impl("fa_forward", q, k, v, o, lse, B, H, H, N, d, scale, causal, 0, nullptr,
+                      stream);
 }
 
 int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int Hq, int Hkv, int N, int d, float scale, int causal, int window,
-                   cudaStream_t stream) {
+                   const float* alibi_slopes, cudaStream_t stream) {
   return forward_impl("fa_forward_gqa", q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, window,
-                      stream);
+                      alibi_slopes, stream);
 }
 
 int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int Hq, int Hkv, int N, int d, float scale, float q_descale, float k_descale,
-                   float v_descale, int causal, int window, void* ws, size_t ws_bytes,
-                   cudaStream_t stream) {
+                   float v_descale, int causal, int window, const float* alibi_slopes,
+                   void* ws, size_t ws_bytes, cudaStream_t stream) {
   const char* fn = "fa_forward_fp8";
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (int r = check_sizes(B, Hq, N, d)) return r;
@@ -212,7 +215,8 @@ int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* 
       return fail(FA_ERR_INVALID_ARG, "%s: descale factors must be finite and > 0", fn);
   if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
     return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
   if (static_cast<long long>(N) > 65535ll * 64 || static_cast<long long>(B) * Hkv > 65535ll)
     return fail(FA_ERR_UNSUPPORTED, "%s: N or B*Hkv too large", fn);
@@ -234,7 +238,8 @@ int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* 
     e = fa::launch_transpose_v_fp8(v, ws, B, Hkv, N, stream);
     if (e == cudaSuccess)
       e = fa::launch_forward_fp8(maps, o, lse, B, Hq, Hkv, N, scale, q_descale, k_descale,
-                                 v_descale, causal, window >= N ? 0 : window, stream, g_events);
+                                 v_descale, causal, window >= N ? 0 : window, alibi_slopes,
+                                 stream, g_events);
   }
   if (own) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
@@ -267,8 +272,8 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o, fl
 static int backward_impl(const char* fn, const void* q, const void* k, const void* v,
                          const void* o, const float* lse, const void* dO, void* dq, void* dk,
                          void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
-                         int causal, int window, void* ws, size_t ws_bytes, bool own_ws,
-                         cudaStream_t stream) {
+                         int causal, int window, const float* alibi, void* ws,
+                         size_t ws_bytes, bool own_ws, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
     return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (int r = check_sizes(B, Hq, N, d)) return r;
@@ -278,8 +283,8 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
   const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
-  if (reinterpret_cast<uintptr_t>(lse) & 3u)
-    return fail(FA_ERR_INVALID_ARG, "%s: lse must be 4-byte aligned", fn);
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(alibi) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s: lse and alibi_slopes must be 4-byte aligned", fn);
   const size_t need = fa::backward_workspace_bytes(B, Hq, N);
   if (!own_ws) {
     if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
@@ -298,8 +303,8 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
     }
   }
   cudaError_t e = fa::launch_backward_bf16(maps, q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N,
-                                           scale, causal, window >= N ? 0 : window, ws, stream,
-                                           g_events);
+                                           scale, causal, window >= N ? 0 : window, alibi, ws,
+                                           stream, g_events);
   if (own_ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = e2;
@@ -311,7 +316,7 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                 float scale, int causal, cudaStream_t stream) {
   return backward_impl("fa_backward", q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale,
-                       causal, 0, nullptr, 0, true, stream);
+                       causal, 0, nullptr, nullptr, 0, true, stream);
 }
 
 int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
@@ -319,15 +324,16 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
                    int N, int d, float scale, int causal, void* ws, size_t ws_bytes,
                    cudaStream_t stream) {
   return backward_impl("fa_backward_ex", q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale,
-                       causal, 0, ws, ws_bytes, false, stream);
+                       causal, 0, nullptr, ws, ws_bytes, false, stream);
 }
 
 int fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
                     int Hq, int Hkv, int N, int d, float scale, int causal, int window,
-                    void* ws, size_t ws_bytes, cudaStream_t stream) {
+                    const float* alibi_slopes, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
   return backward_impl("fa_backward_gqa", q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d,
-                       scale, causal, window, ws, ws_bytes, ws == nullptr, stream);
+                       scale, causal, window, alibi_slopes, ws, ws_bytes, ws == nullptr, stream);
 }
 
 int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,

@@ -41,6 +41,8 @@
 // Sliding window ("03. FlashAttention", "Variantes et extensions"): key k is
 // seen by queries k .. k+w-1, so query blocks past the window of the key
 // block are skipped and the blocks that cut through its edge are masked.
+// ALiBi (same section): the recomputed P includes the bias -slope_h |i - j|
+// (LSE from the forward already does); dS, dQ, dK and dV keep their form.
 #include <cfloat>
 
 #include "fa_device.cuh"
@@ -185,13 +187,17 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 }
 
 // ------------------------------------------------------------------ bwd_main
+// kAlibi: alibi[h] is the ALiBi slope of query head h (h = b*Hq + h' taken
+// modulo heads).
+template <bool kAlibi>
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const float* __restrict__ lse_pad, const float* __restrict__ d_pad,
                 float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dK,
                 __nv_bfloat16* __restrict__ dV, int BHkv, int N, int Npad, float scale,
-                int causal, int qgroup, int window, int head_group) {
+                int causal, int qgroup, int window, int head_group,
+                const float* __restrict__ alibi, int heads) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {           // the swizzled layouts need a 1024-byte aligned base
@@ -402,6 +408,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const int x = it & 1;
       const int st = it % STAGES;
       const int qb = cur.qi * BQ;
+      const float slope_log2 = kAlibi ? alibi[cur.hq % heads] * kLog2e : 0.f;
+      const float d0 = static_cast<float>(qb + sub * 32 - kv);   // query - key at column 0
       const float* stage_lse =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
@@ -430,8 +438,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
         // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
-        const float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
+        float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
         const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
+        if constexpr (kAlibi) {
+          // exponent offset -LSE log2e - slope |i - j| log2e per query column
+          const float de = d0 + static_cast<float>(e);
+          l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
+          l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
+          l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
+          l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
+        }
         float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
         float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
         float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
@@ -541,6 +557,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 size_t padded_len(int N) { return (static_cast<size_t>(N) + PAD - 1) / PAD * PAD; }
 
+template <class K>
+cudaError_t set_smem(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(SMEM_BYTES));
+}
+
 }  // namespace
 
 size_t backward_workspace_bytes(int B, int H, int N) {
@@ -552,16 +574,16 @@ size_t backward_workspace_bytes(int B, int H, int N) {
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H,
-                                 int Hkv, int N, float scale, int causal, int window, void* ws,
-                                 cudaStream_t stream, const TimingEvents& ev) {
+                                 int Hkv, int N, float scale, int causal, int window,
+                                 const float* alibi, void* ws, cudaStream_t stream,
+                                 const TimingEvents& ev) {
   (void)q;
   (void)k;
   (void)v;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
+    cudaError_t e = set_smem(bwd_main_kernel<false>);
+    if (e == cudaSuccess) e = set_smem(bwd_main_kernel<true>);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -583,9 +605,11 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   if (ev.before) cudaEventRecord(ev.before, stream);
   const int g = H / Hkv;
   const int head_group = max(1, kHeadGroup / g);   // about kHeadGroup query heads in flight
-  bwd_main_kernel<<<dim3(nkv * B * Hkv), dim3(NTHREADS), SMEM_BYTES, stream>>>(
+  auto kernel = alibi ? bwd_main_kernel<true> : bwd_main_kernel<false>;
+  kernel<<<dim3(nkv * B * Hkv), dim3(NTHREADS), SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.dO, lse_pad, d_pad, dq_acc, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), B * Hkv, N, Npad, scale, causal, g, window, head_group);
+      static_cast<__nv_bfloat16*>(dv), B * Hkv, N, Npad, scale, causal, g, window, head_group,
+      alibi, H);
   e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;

@@ -27,9 +27,11 @@ int status_forward_fp32(bool clear);
 struct FwdMaps {
   CUtensorMap q, k, v;
 };
+// alibi: device array of H slopes (ALiBi bias -slope_h |i - j|) or nullptr.
 cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
                                 int Hkv, int N, float scale, int causal, int window,
-                                cudaStream_t stream, const TimingEvents& ev);
+                                const float* alibi, cudaStream_t stream,
+                                const TimingEvents& ev);
 int status_forward_bf16(bool clear);
 
 // ---- fp8 (e4m3) tcgen05 forward (fwd_tc.cu).  maps.q, maps.k over
@@ -42,8 +44,8 @@ cudaError_t launch_transpose_v_fp8(const void* v, void* vt, int B, int Hkv, int 
                                    cudaStream_t stream);
 cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, int H, int Hkv,
                                int N, float scale, float q_descale, float k_descale,
-                               float v_descale, int causal, int window, cudaStream_t stream,
-                               const TimingEvents& ev);
+                               float v_descale, int causal, int window, const float* alibi,
+                               cudaStream_t stream, const TimingEvents& ev);
 
 // ---- bf16 backward (bwd_bf16.cu)
 struct BwdMaps {
@@ -54,8 +56,9 @@ size_t backward_workspace_bytes(int B, int H, int N);
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H,
-                                 int Hkv, int N, float scale, int causal, int window, void* ws,
-                                 cudaStream_t stream, const TimingEvents& ev);
+                                 int Hkv, int N, float scale, int causal, int window,
+                                 const float* alibi, void* ws, cudaStream_t stream,
+                                 const TimingEvents& ev);
 int status_backward_bf16(bool clear);
 
 // ---- split-KV decode (decode.cu)

@@ -46,6 +46,9 @@
 // inside the window): query i sees keys i-w+1 .. i.  Each Q block starts at
 // the first key tile that any of its rows sees; tiles that cut through the
 // window's lower edge are masked element-wise like diagonal tiles.
+// ALiBi ("03. FlashAttention", "Variantes et extensions": the linear bias
+// fused into the kernel): -slope_h * |i - j| is added to each scaled score
+// right after it leaves TMEM, before the mask and the online softmax.
 // FP8 ("03. FlashAttention", "FlashAttention v3": the FP8 format as a
 // hardware lever): Q, K, V in e4m3 with per-tensor descale factors; the
 // same loop runs kind::f8f6f4 products (K = 32 per instruction, twice the
@@ -217,14 +220,17 @@ struct Ctx {
 };
 
 // The kernel body for element type T.  kWindow: a sliding window is applied
-// (window >= 1); the plain instantiation carries none of its bookkeeping.
-// out_scale multiplies O at the end (the fp8 V descale; 1 for bf16).
-template <class T, bool kWindow>
+// (window >= 1); kAlibi: the ALiBi bias -slope_h * |i - j| is added to the
+// scaled scores (alibi[h] = slope of query head h, h = bh % heads).  The
+// plain instantiation carries none of their bookkeeping.  out_scale
+// multiplies O at the end (the fp8 V descale; 1 for bf16).
+template <class T, bool kWindow, bool kAlibi>
 __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                          const CUtensorMap* tmV, __nv_bfloat16* __restrict__ O,
                                          float* __restrict__ LSE, int BH, int N,
                                          float scale_log2, float out_scale, int causal,
-                                         int group, int window) {
+                                         int group, int window, const float* __restrict__ alibi,
+                                         int heads) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -387,6 +393,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     float m = -INFINITY;                          // reference max, log2 units
     float l = 0.f;                                // running sum
     bool ok = true;
+    // ALiBi scales and biases the scores in place; the max and the
+    // exponentials then take them as they are.
+    const float slope_log2 = kAlibi ? alibi[bh % heads] * 1.4426950408889634f : 0.f;
+    const float sl = kAlibi ? 1.f : scale_log2;
 
     for (int j = lo; j < nt; ++j) {
       if (!ctx.wait(T::B_SFULL + blk, (j - lo) & 1)) {
@@ -400,6 +410,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         tmem_ld128(s_addr, r);                    // the row's 128 scores in one round trip
 #pragma unroll
         for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
+      }
+      if constexpr (kAlibi) {
+        const float d0 = static_cast<float>(j * BN - q_row);   // key - query at column 0
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          s[c] = fmaf(s[c], scale_log2, -slope_log2 * fabsf(d0 + static_cast<float>(c)));
       }
       // mask: causal diagonal tile, keys past the end of the sequence, or a
       // tile that cuts through the window's lower edge
@@ -436,7 +452,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
 #pragma unroll
         for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
       }
-      mx *= scale_log2;
+      mx *= sl;
       // Raise the reference max only when the new one exceeds it by more
       // than the threshold (always on the first tile, where m = -inf).
       float corr = 1.f;
@@ -454,11 +470,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       uint32_t pk[T::P_COLS];
 #pragma unroll
       for (int c = 0; c < BN / 4; ++c) {
-        const float p0 = fast_exp2(fmaf(s[4 * c], scale_log2, -mref));
-        const float p1 = fast_exp2(fmaf(s[4 * c + 1], scale_log2, -mref));
+        const float p0 = fast_exp2(fmaf(s[4 * c], sl, -mref));
+        const float p1 = fast_exp2(fmaf(s[4 * c + 1], sl, -mref));
         if constexpr (!T::kSplitChains) rsp[0] += p0 + p1;
-        const float p2 = fast_exp2(fmaf(s[4 * c + 2], scale_log2, -mref));
-        const float p3 = fast_exp2(fmaf(s[4 * c + 3], scale_log2, -mref));
+        const float p2 = fast_exp2(fmaf(s[4 * c + 2], sl, -mref));
+        const float p3 = fast_exp2(fmaf(s[4 * c + 3], sl, -mref));
         if constexpr (T::kSplitChains)
           rsp[c & 3] += (p0 + p1) + (p2 + p3);
         else
@@ -518,26 +534,26 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
   }
 }
 
-// kWindow: a sliding window is applied (window >= 1).
-template <bool kWindow>
+// kWindow: a sliding window is applied (window >= 1); kAlibi: ALiBi bias.
+template <bool kWindow, bool kAlibi>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
                 float* __restrict__ LSE, int BH, int N, float scale_log2, int causal,
-                int group, int window) {
-  fwd_body<Bf16, kWindow>(&tmQ, &tmK, &tmV, O, LSE, BH, N, scale_log2, 1.f, causal, group,
-                          window);
+                int group, int window, const float* __restrict__ alibi, int heads) {
+  fwd_body<Bf16, kWindow, kAlibi>(&tmQ, &tmK, &tmV, O, LSE, BH, N, scale_log2, 1.f, causal,
+                                  group, window, alibi, heads);
 }
 
 // Q, K e4m3 [BH, N, 128]; tmV maps the transposed copy V^T [BH, 128, keys].
-template <bool kWindow>
+template <bool kWindow, bool kAlibi>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmVt, __nv_bfloat16* __restrict__ O,
                float* __restrict__ LSE, int BH, int N, float scale_log2, float v_descale,
-               int causal, int group, int window) {
-  fwd_body<Fp8, kWindow>(&tmQ, &tmK, &tmVt, O, LSE, BH, N, scale_log2, v_descale, causal, group,
-                         window);
+               int causal, int group, int window, const float* __restrict__ alibi, int heads) {
+  fwd_body<Fp8, kWindow, kAlibi>(&tmQ, &tmK, &tmVt, O, LSE, BH, N, scale_log2, v_descale,
+                                 causal, group, window, alibi, heads);
 }
 
 // V [rows, 128] e4m3 -> V^T [128, ld] per head, 64 keys x 128 columns per
@@ -600,22 +616,27 @@ cudaError_t set_smem(K kernel, uint32_t bytes) {
 
 cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
                                 int Hkv, int N, float scale, int causal, int window,
-                                cudaStream_t stream, const TimingEvents& ev) {
+                                const float* alibi, cudaStream_t stream,
+                                const TimingEvents& ev) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = set_smem(fwd_bf16_kernel<false>, Bf16::SMEM_BYTES);
-    if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<true>, Bf16::SMEM_BYTES);
+    cudaError_t e = set_smem(fwd_bf16_kernel<false, false>, Bf16::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<true, false>, Bf16::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<false, true>, Bf16::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<true, true>, Bf16::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int BH = B * H;
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const float scale_log2 = scale * 1.4426950408889634f;
-  auto kernel = window > 0 ? fwd_bf16_kernel<true> : fwd_bf16_kernel<false>;
+  auto kernel = alibi ? (window > 0 ? fwd_bf16_kernel<true, true> : fwd_bf16_kernel<false, true>)
+                      : (window > 0 ? fwd_bf16_kernel<true, false>
+                                    : fwd_bf16_kernel<false, false>);
   if (ev.before) cudaEventRecord(ev.before, stream);
   kernel<<<dim3(npair * BH), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal,
-      H / Hkv, window);
+      H / Hkv, window, alibi, H);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;
@@ -637,23 +658,26 @@ cudaError_t launch_transpose_v_fp8(const void* v, void* vt, int B, int Hkv, int 
 
 cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, int H, int Hkv,
                                int N, float scale, float q_descale, float k_descale,
-                               float v_descale, int causal, int window, cudaStream_t stream,
-                               const TimingEvents& ev) {
+                               float v_descale, int causal, int window, const float* alibi,
+                               cudaStream_t stream, const TimingEvents& ev) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = set_smem(fwd_fp8_kernel<false>, Fp8::SMEM_BYTES);
-    if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<true>, Fp8::SMEM_BYTES);
+    cudaError_t e = set_smem(fwd_fp8_kernel<false, false>, Fp8::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<true, false>, Fp8::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<false, true>, Fp8::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<true, true>, Fp8::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int BH = B * H;
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const float scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
-  auto kernel = window > 0 ? fwd_fp8_kernel<true> : fwd_fp8_kernel<false>;
+  auto kernel = alibi ? (window > 0 ? fwd_fp8_kernel<true, true> : fwd_fp8_kernel<false, true>)
+                      : (window > 0 ? fwd_fp8_kernel<true, false> : fwd_fp8_kernel<false, false>);
   if (ev.before) cudaEventRecord(ev.before, stream);
   kernel<<<dim3(npair * BH), dim3(NTHREADS), Fp8::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, v_descale,
-      causal, H / Hkv, window);
+      causal, H / Hkv, window, alibi, H);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;

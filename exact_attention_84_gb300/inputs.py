@@ -100,6 +100,12 @@ def gqa_inputs(B, Hq, Hkv, N, d, dtype, seed, device, with_do=False):
     return q, k, v
 
 
+def alibi_slopes(H, device):
+    """The usual ALiBi slope schedule m_h = 2^(-8 (h + 1) / H), fp32 [H]."""
+    h = torch.arange(1, H + 1, dtype=torch.float64)
+    return torch.pow(2.0, -8.0 * h / H).to(torch.float32).to(device)
+
+
 def fp8_inputs(B, Hq, Hkv, N, d, seed, device, amp=FP8_AMP):
     """E4M3 codes as uint8: q [B, Hq, N, d], k, v [B, Hkv, N, d], each drawn
     as fp32 N(0,1) times `amp` and rounded to E4M3 (values stay far below

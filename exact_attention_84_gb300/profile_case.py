@@ -78,14 +78,15 @@ def main():
 
         def call():
             _lib.check(_lib.fa_forward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                           lse.data_ptr(), B, H, H, N, d, scale, 1, W, sh))
+                                           lse.data_ptr(), B, H, H, N, d, scale, 1, W, None,
+                                           sh))
     elif a.case == "bwd_gqa":
         B, Hq, Hkv, N = 2, 32, 8, 4096
         q, k, v, do = inputs.gqa_inputs(B, Hq, Hkv, N, d, torch.bfloat16, 5, dev, with_do=True)
         o = torch.empty_like(q)
         lse = torch.empty((B, Hq, N), device=dev, dtype=torch.float32)
         _lib.check(_lib.fa_forward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                       lse.data_ptr(), B, Hq, Hkv, N, d, scale, 1, 0, sh))
+                                       lse.data_ptr(), B, Hq, Hkv, N, d, scale, 1, 0, None, sh))
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         nbytes = _lib.fa_workspace_size(_lib.FA_OP_BACKWARD, B, Hq, N, d, 0)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -94,7 +95,8 @@ def main():
             _lib.check(_lib.fa_backward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                             o.data_ptr(), lse.data_ptr(), do.data_ptr(),
                                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq,
-                                            Hkv, N, d, scale, 1, 0, ws.data_ptr(), nbytes, sh))
+                                            Hkv, N, d, scale, 1, 0, None, ws.data_ptr(), nbytes,
+                                            sh))
     elif a.case == "dec_gqa":
         B, Hq, Hkv, L, S = 4, 32, 8, 32768, 8
         q, kc, vc = inputs.decode_gqa_inputs(B, Hq, Hkv, L, d, torch.bfloat16, 7, dev)

@@ -113,11 +113,17 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o,
  *   window   0: none.  >= 1 needs causal == 1 (FA_ERR_UNSUPPORTED
  *            otherwise); a window >= N is the same as none.  < 0:
  *            FA_ERR_INVALID_ARG.
+ *   alibi_slopes  NULL, or a DEVICE array of Hq fp32 slopes m_h (4-byte
+ *            aligned): ALiBi ("03. FlashAttention", "Variantes et
+ *            extensions": the linear bias fused into the kernel) adds
+ *            -m_h * |i - j| to the scaled score of query i and key j of
+ *            query head h before the softmax (under the causal mask this
+ *            is m_h * (j - i)); LSE includes the bias.
  *   Other arguments as in fa_forward.  Allocates nothing.
  */
 int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                   int window, cudaStream_t stream);
+                   int window, const float* alibi_slopes, cudaStream_t stream);
 
 /*
  * fa_forward_fp8 -- the forward pass with 8-bit floating-point inputs
@@ -132,7 +138,7 @@ int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* 
  * of at most 2^-4 relative to each weight.  o is bf16, lse fp32 (natural
  * log), as in fa_forward.
  *
- *   Hkv, causal, window  as in fa_forward_gqa.
+ *   Hkv, causal, window, alibi_slopes  as in fa_forward_gqa.
  *   descale factors      finite and > 0.
  *   ws                   NULL: a workspace (a transposed copy of V) comes
  *                        from the library pool; otherwise a caller buffer of
@@ -142,8 +148,9 @@ int fa_forward_gqa(const void* q, const void* k, const void* v, void* o, float* 
  */
 int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int Hq, int Hkv, int N, int d, float scale, float q_descale,
-                   float k_descale, float v_descale, int causal, int window, void* ws,
-                   size_t ws_bytes, cudaStream_t stream);
+                   float k_descale, float v_descale, int causal, int window,
+                   const float* alibi_slopes, void* ws, size_t ws_bytes,
+                   cudaStream_t stream);
 
 /*
  * fa_backward -- gradients dQ, dK, dV by recomputation.
@@ -183,8 +190,9 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
                    int causal, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
- * fa_backward_gqa -- fa_backward with grouped query heads and an optional
- * causal sliding window (same meaning as in fa_forward_gqa).  dK and dV of a
+ * fa_backward_gqa -- fa_backward with grouped query heads, an optional
+ * causal sliding window and optional ALiBi slopes (same meaning as in
+ * fa_forward_gqa; the slopes must match the forward call's).  dK and dV of a
  * key/value head are the sums of the gradients of its g query heads.
  *
  *   q, o, dO, dq  [B,Hq,N,d] bf16;  k, v, dk, dv [B,Hkv,N,d] bf16;
@@ -198,7 +206,8 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
 int fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                    int window, void* ws, size_t ws_bytes, cudaStream_t stream);
+                    int window, const float* alibi_slopes, void* ws, size_t ws_bytes,
+                    cudaStream_t stream);
 
 /*
  * fa_decode -- split-KV attention of one new query token per sequence over

@@ -44,11 +44,11 @@ def decode_e4m3(codes) -> np.ndarray:
 
 
 def attention_forward_fp8(q8, k8, v8, scale: float, q_descale: float, k_descale: float,
-                          v_descale: float, causal: bool, window=None):
+                          v_descale: float, causal: bool, window=None, alibi_slopes=None):
     """q8 [B, Hq, N, d], k8/v8 [B, Hkv, N, d] E4M3 codes -> (O, LSE) of
     attention over Q = q_descale*decode(q8), K = k_descale*decode(k8),
     V = v_descale*decode(v8)."""
     q = decode_e4m3(q8) * q_descale
     k = decode_e4m3(k8) * k_descale
     v = decode_e4m3(v8) * v_descale
-    return attention_forward_gqa(q, k, v, scale, causal, window)
+    return attention_forward_gqa(q, k, v, scale, causal, window, alibi_slopes)

@@ -83,20 +83,30 @@ def test_gqa_window_validation(lib):
     E = _lib
     f = E.fa_forward_gqa
     # Hq must be a multiple of Hkv
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 6, 4, 8, 128, 0.1, 1, 0, None) == E.FA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 6, 4, 8, 128, 0.1, 1, 0, None, None) == E.FA_ERR_INVALID_ARG
     assert "multiple" in E.fa_last_error()
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 0, 8, 128, 0.1, 1, 0, None) == E.FA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 0, 8, 128, 0.1, 1, 0, None, None) == E.FA_ERR_INVALID_ARG
     # a window needs the causal mask; negative windows are invalid
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 128, 0.1, 0, 4, None) == E.FA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 128, 0.1, 0, 4, None, None) == E.FA_ERR_UNSUPPORTED
     assert "causal" in E.fa_last_error()
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 128, 0.1, 1, -1, None) == E.FA_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 64, 0.1, 1, 4, None) == E.FA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 128, 0.1, 1, -1, None, None) == E.FA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 64, 0.1, 1, 4, None, None) == E.FA_ERR_UNSUPPORTED
     args = [FAKE] * 9
     b = E.fa_backward_gqa
-    assert b(*args, 1, 4, 3, 8, 128, 0.1, 1, 0, None, 0, None) == E.FA_ERR_INVALID_ARG
-    assert b(*args, 1, 4, 2, 8, 128, 0.1, 0, 2, None, 0, None) == E.FA_ERR_UNSUPPORTED
-    assert b(*args, 1, 4, 2, 8, 128, 0.1, 1, 2, FAKE, 16, None) == E.FA_ERR_INVALID_ARG
+    assert b(*args, 1, 4, 3, 8, 128, 0.1, 1, 0, None, None, 0, None) == E.FA_ERR_INVALID_ARG
+    assert b(*args, 1, 4, 2, 8, 128, 0.1, 0, 2, None, None, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert b(*args, 1, 4, 2, 8, 128, 0.1, 1, 2, None, FAKE, 16, None) == E.FA_ERR_INVALID_ARG
     assert "workspace" in E.fa_last_error()
+    # misaligned slopes
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 128, 0.1, 1, 0, MIS, None) == E.FA_ERR_INVALID_ARG
+    p8 = E.fa_forward_fp8
+    assert p8(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 8, 128, 0.1, 1.0, 0.0, 1.0, 1, 0, None, None, 0,
+              None) == E.FA_ERR_INVALID_ARG
+    assert "descale" in E.fa_last_error()
+    assert p8(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 8, 128, 0.1, 1.0, 1.0, 1.0, 0, 3, None, None, 0,
+              None) == E.FA_ERR_UNSUPPORTED
+    assert p8(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 8, 128, 0.1, 1.0, 1.0, 1.0, 1, 0, None, FAKE, 8,
+              None) == E.FA_ERR_INVALID_ARG
     d = E.fa_decode_gqa
     assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 3, 100, 128, 2, 0.1, None, 0, None) == E.FA_ERR_INVALID_ARG
     assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 0, 0.1, None, 0, None) == E.FA_ERR_INVALID_ARG
