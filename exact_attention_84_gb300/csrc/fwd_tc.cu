@@ -413,9 +413,17 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       }
       if constexpr (kAlibi) {
         const float d0 = static_cast<float>(j * BN - q_row);   // key - query at column 0
+        if (causal) {
+          // every key the mask leaves has key <= query: -|i - j| = j - i
+          const float base = slope_log2 * d0;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
-          s[c] = fmaf(s[c], scale_log2, -slope_log2 * fabsf(d0 + static_cast<float>(c)));
+          for (int c = 0; c < BN; ++c)
+            s[c] = fmaf(s[c], scale_log2, fmaf(slope_log2, static_cast<float>(c), base));
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            s[c] = fmaf(s[c], scale_log2, -slope_log2 * fabsf(d0 + static_cast<float>(c)));
+        }
       }
       // mask: causal diagonal tile, keys past the end of the sequence, or a
       // tile that cuts through the window's lower edge
