@@ -474,7 +474,7 @@ def measure_targets(args, dev, peaks, peak_src):
     bwd = lambda: _lib.check(_lib.fa_backward_gqa(  # noqa: E731
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, hkv, w.N, w.d, scale, 1, 0,
-        None, ws.data_ptr(), ws.numel(), sh))
+        None, 0, ws.data_ptr(), ws.numel(), sh))
     fl = acc.forward_flops(w.B, w.H, w.N, w.d, True)
     for key, call, flops in (("forward_gqa_causal_B8_Hq32_Hkv8_N4096", fwd, fl),
                              ("backward_gqa_causal_B8_Hq32_Hkv8_N4096", bwd, 2.5 * fl)):

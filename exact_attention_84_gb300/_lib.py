@@ -35,7 +35,7 @@ SIGNATURES = {
     "fa_forward_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I,
                             _P, _P, _Z, _P]),
     "fa_backward_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
-                             _I, _P, _P, _Z, _P]),
+                             _I, _P, _I, _P, _Z, _P]),
     "fa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "fa_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_backward_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I,
@@ -105,9 +105,9 @@ def fa_forward_fp8(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, q_descale, k_descal
 
 
 def fa_backward_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window,
-                    alibi_slopes, ws, ws_bytes, stream):
+                    alibi_slopes, deterministic, ws, ws_bytes, stream):
     return _call("fa_backward_gqa", q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, scale,
-                 causal, window, alibi_slopes, ws, ws_bytes, stream)
+                 causal, window, alibi_slopes, deterministic, ws, ws_bytes, stream)
 
 
 def fa_decode_gqa(q, kcache, vcache, o, lse_out, B, Hq, Hkv, Lkv, d, num_splits, scale, ws,

@@ -84,11 +84,13 @@ def forward_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-             workspace=None, out=None, window: int = 0, alibi_slopes=None):
+             workspace=None, out=None, window: int = 0, alibi_slopes=None,
+             deterministic: bool = False):
     """dQ, dK, dV for bf16 [B, H, N, d] tensors; lse from ``forward``.
     ``out`` may hold three preallocated tensors (dq, dk, dv) to write into.
-    k, v (and dk, dv) may have fewer heads, and ``window`` applies, as in
-    ``forward``."""
+    k, v (and dk, dv) may have fewer heads, and ``window`` / ``alibi_slopes``
+    apply, as in ``forward``.  ``deterministic``: bitwise-reproducible dQ
+    (no atomics)."""
     B, H, N, d = q.shape
     Hkv = k.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -104,12 +106,12 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
     args = ptrs + (B, H, N, d, scale, int(causal))
-    if Hkv != H or window or alibi_slopes is not None:
+    if Hkv != H or window or alibi_slopes is not None or deterministic:
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
         _lib.check(_lib.fa_backward_gqa(*ptrs, B, H, Hkv, N, d, scale, int(causal), int(window),
-                                        _slopes(alibi_slopes, H), ws_ptr, ws_bytes,
-                                        _stream()))
+                                        _slopes(alibi_slopes, H), int(deterministic), ws_ptr,
+                                        ws_bytes, _stream()))
     elif workspace is None:
         _lib.check(_lib.fa_backward(*args, _stream()))
     else:

@@ -272,8 +272,8 @@ int fa_forward_fp32(const float* q, const float* k, const float* v, float* o, fl
 static int backward_impl(const char* fn, const void* q, const void* k, const void* v,
                          const void* o, const float* lse, const void* dO, void* dq, void* dk,
                          void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
-                         int causal, int window, const float* alibi, void* ws,
-                         size_t ws_bytes, bool own_ws, cudaStream_t stream) {
+                         int causal, int window, const float* alibi, int deterministic,
+                         void* ws, size_t ws_bytes, bool own_ws, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv)
     return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (int r = check_sizes(B, Hq, N, d)) return r;
@@ -291,11 +291,19 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
       return fail(FA_ERR_INVALID_ARG,
                   "%s: workspace must be 256-byte aligned and >= %zu bytes", fn, need);
   }
-  fa::BwdMaps maps;
+  if (deterministic != 0 && deterministic != 1)
+    return fail(FA_ERR_INVALID_ARG, "%s: deterministic must be 0 or 1", fn);
+  fa::BwdMaps maps, dq_maps;
   if (int r = make_map(&maps.q, q, B * Hq, N, 64)) return r;     // 64-query blocks
   if (int r = make_map(&maps.dO, dO, B * Hq, N, 64)) return r;
   if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
+  if (deterministic) {                                            // 128-query blocks, 64-key tiles
+    if (int r = make_map(&dq_maps.q, q, B * Hq, N, 128)) return r;
+    if (int r = make_map(&dq_maps.dO, dO, B * Hq, N, 128)) return r;
+    if (int r = make_map(&dq_maps.k, k, B * Hkv, N, 64)) return r;
+    if (int r = make_map(&dq_maps.v, v, B * Hkv, N, 64)) return r;
+  }
   if (own_ws) {
     if (workspace_alloc(&ws, need, stream) != cudaSuccess) {
       cudaGetLastError();
@@ -303,8 +311,9 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
     }
   }
   cudaError_t e = fa::launch_backward_bf16(maps, q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N,
-                                           scale, causal, window >= N ? 0 : window, alibi, ws,
-                                           stream, g_events);
+                                           scale, causal, window >= N ? 0 : window, alibi,
+                                           deterministic ? &dq_maps : nullptr, ws, stream,
+                                           g_events);
   if (own_ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = e2;
@@ -316,7 +325,7 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
                 const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                 float scale, int causal, cudaStream_t stream) {
   return backward_impl("fa_backward", q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale,
-                       causal, 0, nullptr, nullptr, 0, true, stream);
+                       causal, 0, nullptr, 0, nullptr, 0, true, stream);
 }
 
 int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
@@ -324,16 +333,17 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
                    int N, int d, float scale, int causal, void* ws, size_t ws_bytes,
                    cudaStream_t stream) {
   return backward_impl("fa_backward_ex", q, k, v, o, lse, dO, dq, dk, dv, B, H, H, N, d, scale,
-                       causal, 0, nullptr, ws, ws_bytes, false, stream);
+                       causal, 0, nullptr, 0, ws, ws_bytes, false, stream);
 }
 
 int fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
                     int Hq, int Hkv, int N, int d, float scale, int causal, int window,
-                    const float* alibi_slopes, void* ws, size_t ws_bytes,
+                    const float* alibi_slopes, int deterministic, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
   return backward_impl("fa_backward_gqa", q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d,
-                       scale, causal, window, alibi_slopes, ws, ws_bytes, ws == nullptr, stream);
+                       scale, causal, window, alibi_slopes, deterministic, ws, ws_bytes,
+                       ws == nullptr, stream);
 }
 
 int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,

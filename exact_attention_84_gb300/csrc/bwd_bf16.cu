@@ -161,9 +161,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       s = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), s);
       s = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(bw[i] & 0xffff0000u), s);
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + row * HD + sub * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dq_acc != nullptr) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * HD + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -188,8 +190,9 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 
 // ------------------------------------------------------------------ bwd_main
 // kAlibi: alibi[h] is the ALiBi slope of query head h (h = b*Hq + h' taken
-// modulo heads).
-template <bool kAlibi>
+// modulo heads).  kDq: this kernel also forms dQ (fp32 atomics into dq_acc);
+// without it only dK and dV are made and dQ is left to bwd_dq_kernel.
+template <bool kAlibi, bool kDq>
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -343,7 +346,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
         tc_fence_after();
         // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
-        {
+        if constexpr (kDq) {
           const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
           uint64_t a[8], b[8];
 #pragma unroll
@@ -352,8 +355,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             b[kk] = dsd + ((kk * 2048) >> 4);
           }
           mma_ss_batch8(r1(it), a, b, IDESC_DQ, 0u);
+          mma_commit(bar_addr(sbase, B_DQFULL + x));
         }
-        mma_commit(bar_addr(sbase, B_DQFULL + x));
         // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
         // P^T packed in columns [32g, 32g+16) and dS^T in [32g+16, 32g+32);
         // 16 queries = 8 packed columns.
@@ -380,8 +383,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           tc_fence_after();
           issue_sdp(it + 2, false);
           // R1_X holds dQ^T(i) until the writers have read it.
-          if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
-          tc_fence_after();
+          if constexpr (kDq) {
+            if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
+            tc_fence_after();
+          }
           issue_sdp(it + 2, true);
           mma_commit(bar_addr(sbase, B_SFULL + x));
         }
@@ -473,14 +478,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tmem_st16(s_addr, pk);
       tmem_st16(s_addr + 16, gk);
       // dS^T row into this block's shared buffer (MN-major operand of dQ^T).
-      uint8_t* ds_smem = smem + OFF_DS + x * DS_TILE;
+      if constexpr (kDq) {
+        uint8_t* ds_smem = smem + OFF_DS + x * DS_TILE;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t off = sw128_offset(row, sub * 4 + ch);
-        *reinterpret_cast<uint4*>(ds_smem + off) =
-            make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t off = sw128_offset(row, sub * 4 + ch);
+          *reinterpret_cast<uint4*>(ds_smem + off) =
+              make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -509,7 +516,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
       }
     }
-  } else {
+  } else if (kDq) {
     // ------------------------------------------------------------ dQ writers
     const int quad = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
@@ -555,12 +562,276 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
+// ------------------------------------------------------------------ bwd_dq
+// Deterministic dQ (the dQ half of the gradient without atomics): one thread
+// block per (query head, 128-query block i), K_j / V_j streamed in 64-key
+// tiles in increasing key order, dQ_i accumulated in TMEM and written once:
+//   S = Q_i K_j^T, dP = dO_i V_j^T            (shared-memory operands)
+//   P = exp2(S scale log2e - LSE log2e [- ALiBi]),  dS = P * (dP - D)
+//   dQ_i += dS K_j                             (dS from TMEM, K_j MN-major)
+// Two TMEM buffers of [S | dP] let the softmax of tile t overlap the
+// products of tiles t-1 and t+1.  Each dQ element is summed by one thread
+// block in a fixed order, so the result is the same on every run.
+constexpr int DQ_BQ = 128;                     // query rows (TMEM lanes)
+constexpr int DQ_BK = 64;                      // keys per tile
+constexpr int DQ_STAGES = 4;
+constexpr uint32_t DQ_QTILE = DQ_BQ * HD * 2;  // Q_i or dO_i: 32 KiB
+constexpr uint32_t DQ_QHALF = DQ_QTILE / 2;    // 128 rows x 64 columns
+constexpr uint32_t DQ_KTILE = DQ_BK * HD * 2;  // K_j or V_j: 16 KiB
+constexpr uint32_t DQ_KHALF = DQ_KTILE / 2;    // 64 rows x 64 columns
+constexpr uint32_t DQ_OFF_Q = 0;
+constexpr uint32_t DQ_OFF_DO = DQ_QTILE;
+constexpr uint32_t DQ_OFF_RING = 2 * DQ_QTILE;
+constexpr uint32_t DQ_STAGE = 2 * DQ_KTILE;    // K_j then V_j
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
+constexpr int DQB_QFULL = 0;
+constexpr int DQB_FULL = 1;                          // + stage
+constexpr int DQB_EMPTY = DQB_FULL + DQ_STAGES;      // + stage
+constexpr int DQB_SFULL = DQB_EMPTY + DQ_STAGES;     // + buffer
+constexpr int DQB_PFULL = DQB_SFULL + 2;             // + buffer (8 warps)
+constexpr int DQB_DONE = DQB_PFULL + 2;
+constexpr int DQ_NBAR = DQB_DONE + 1;
+constexpr uint32_t DQ_OFF_MISC = DQ_OFF_BAR + DQ_NBAR * 8;
+constexpr uint32_t DQ_SMEM = DQ_OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
+constexpr int DQ_THREADS = 320;                // 0-7 softmax, 8 producer, 9 MMA
+constexpr uint32_t DQ_TM_DQ = 256;             // buffer x: S at 128x, dP at 128x + 64
+constexpr uint32_t IDESC_DQ_S = idesc_bf16(DQ_BQ, DQ_BK, false, false);
+constexpr uint32_t IDESC_DQ_ACC = idesc_bf16(DQ_BQ, HD, false, true);
+
+template <bool kAlibi>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+              const float* __restrict__ lse_pad, const float* __restrict__ d_pad,
+              __nv_bfloat16* __restrict__ dQ, int BH, int N, int Npad, float scale, int causal,
+              int group, int window, const float* __restrict__ alibi, int heads) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + DQ_OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_MISC + 4);
+  auto bar = [&](int i) { return sbase + DQ_OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  auto wait = [&](int i, uint32_t parity) {
+    return mbar_wait(bar(i), parity, abort_flag, &g_status_bwd);
+  };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int npb = (N + DQ_BQ - 1) / DQ_BQ;
+  const int qblk = causal ? npb - 1 - static_cast<int>(blockIdx.x) / BH
+                          : static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int bkv = bh / group;
+  const int q0 = qblk * DQ_BQ;
+  // keys seen by some row of the block: [key_lo, key_hi)
+  const int key_lo = window > 0 ? max(0, q0 - window + 1) : 0;
+  const int key_hi = causal ? min(N, q0 + DQ_BQ) : N;
+  const int t_lo = key_lo / DQ_BK;
+  const int nt = (key_hi + DQ_BK - 1) / DQ_BK - t_lo;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(DQB_QFULL), 1);
+    for (int s = 0; s < DQ_STAGES; ++s) {
+      mbar_init(bar(DQB_FULL + s), 1);
+      mbar_init(bar(DQB_EMPTY + s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(DQB_SFULL + x), 1);
+      mbar_init(bar(DQB_PFULL + x), 8);
+    }
+    mbar_init(bar(DQB_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmdO);
+      const uint32_t qf = bar(DQB_QFULL);
+      mbar_arrive_expect_tx(qf, 2 * DQ_QTILE);
+      tma_load_3d(sbase + DQ_OFF_Q, &tmQ, qf, 0, q0, bh);
+      tma_load_3d(sbase + DQ_OFF_Q + DQ_QHALF, &tmQ, qf, 64, q0, bh);
+      tma_load_3d(sbase + DQ_OFF_DO, &tmdO, qf, 0, q0, bh);
+      tma_load_3d(sbase + DQ_OFF_DO + DQ_QHALF, &tmdO, qf, 64, q0, bh);
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % DQ_STAGES;
+        if (t >= DQ_STAGES && !wait(DQB_EMPTY + st, ((t / DQ_STAGES) - 1) & 1)) break;
+        const uint32_t fb = bar(DQB_FULL + st);
+        const uint32_t dst = sbase + DQ_OFF_RING + st * DQ_STAGE;
+        const int key = (t_lo + t) * DQ_BK;
+        mbar_arrive_expect_tx(fb, DQ_STAGE);
+        tma_load_3d(dst, &tmK, fb, 0, key, bkv);
+        tma_load_3d(dst + DQ_KHALF, &tmK, fb, 64, key, bkv);
+        tma_load_3d(dst + DQ_KTILE, &tmV, fb, 0, key, bkv);
+        tma_load_3d(dst + DQ_KTILE + DQ_KHALF, &tmV, fb, 64, key, bkv);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
+      auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
+      // S(t) into buffer t & 1 and dP(t) beside it: reductions over d.
+      auto issue_sdp = [&](int t) {
+        const uint32_t buf = tmem + 128u * (t & 1);
+        const uint64_t qd = sdesc_sw128(sbase + DQ_OFF_Q, 16, 1024);
+        const uint64_t dod = sdesc_sw128(sbase + DQ_OFF_DO, 16, 1024);
+        const uint64_t kd = sdesc_sw128(ring(t), 16, 1024);
+        const uint64_t vd = sdesc_sw128(ring(t) + DQ_KTILE, 16, 1024);
+        uint64_t a[8], b[8], a2[8], b2[8];
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t oa = ((kk >> 2) * DQ_QHALF + (kk & 3) * 32) >> 4;
+          const uint64_t ob = ((kk >> 2) * DQ_KHALF + (kk & 3) * 32) >> 4;
+          a[kk] = qd + oa;
+          b[kk] = kd + ob;
+          a2[kk] = dod + oa;
+          b2[kk] = vd + ob;
+        }
+        mma_ss_batch8(buf, a, b, IDESC_DQ_S, 0u);
+        mma_ss_batch8(buf + 64, a2, b2, IDESC_DQ_S, 0u);
+      };
+      bool ok = wait(DQB_QFULL, 0);
+      for (int t = 0; t < 2 && t < nt && ok; ++t) {
+        if (!(ok = full(t))) break;
+        tc_fence_after();
+        issue_sdp(t);
+        mma_commit(bar(DQB_SFULL + t));
+      }
+      for (int t = 0; t < nt && ok; ++t) {
+        const int x = t & 1;
+        if (!(ok = wait(DQB_PFULL + x, (t >> 1) & 1))) break;
+        tc_fence_after();
+        // dQ += dS K_t: dS packed in TMEM (keys 0-31 in columns [0, 16),
+        // keys 32-63 in [32, 48) of the buffer), K_t MN-major (16 keys =
+        // 2048 bytes per step, 64-column blocks 8 KiB apart).
+        {
+          const uint64_t kd = sdesc_sw128(ring(t), DQ_KHALF, 1024);
+          uint32_t a[4];
+          uint64_t b[4];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            a[kk] = tmem + 128u * x + 32 * (kk >> 1) + 8 * (kk & 1);
+            b[kk] = kd + ((kk * 2048) >> 4);
+          }
+          mma_ts_batch4(tmem + DQ_TM_DQ, a, b, IDESC_DQ_ACC, t > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(DQB_EMPTY + t % DQ_STAGES));
+        if (t + 2 < nt) {
+          if (!(ok = full(t + 2))) break;
+          tc_fence_after();
+          issue_sdp(t + 2);           // after dQ(t) has read dS(t) (in issue order)
+          mma_commit(bar(DQB_SFULL + x));
+        }
+      }
+      if (ok) mma_commit(bar(DQB_DONE));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Warp w: TMEM lane quadrant w & 3 (query rows), key half w >> 2.
+    const int quad = warp & 3, sub = warp >> 2;
+    const int row = quad * 32 + lane;
+    const int q = q0 + row;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const bool row_valid = q < N;
+    const size_t srow = static_cast<size_t>(bh) * Npad + q;      // q < Npad always
+    const float nlse = lse_pad[srow];                            // -LSE log2e
+    const float nd = d_pad[srow];                                // -D
+    const float scale_log2 = scale * kLog2e;
+    const float slope_log2 = kAlibi ? alibi[bh % heads] * kLog2e : 0.f;
+    // keys this row sees: [lo, hi]
+    const int lo = window > 0 ? q - window + 1 : 0;
+    const int hi = causal ? min(q, N - 1) : N - 1;
+    bool ok = true;
+    for (int t = 0; t < nt; ++t) {
+      const int x = t & 1;
+      if (!wait(DQB_SFULL + x, (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t s_addr = tmem + lane_addr + 128u * x + 32 * sub;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(s_addr, sr);
+      tmem_ld32(s_addr + 64, dr);
+      const int j0 = (t_lo + t) * DQ_BK + 32 * sub;               // first key of this half
+      const bool need_mask = !row_valid || j0 < lo || j0 + 31 > hi;
+      const float d0 = static_cast<float>(q - j0);
+      uint32_t gk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float b0 = nlse, b1 = nlse;
+        if constexpr (kAlibi) {
+          b0 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e)), nlse);
+          b1 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e + 1)), nlse);
+        }
+        float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, b0));
+        float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, b1));
+        if (need_mask) {
+          const bool v0 = row_valid && j0 + e >= lo && j0 + e <= hi;
+          const bool v1 = row_valid && j0 + e + 1 >= lo && j0 + e + 1 <= hi;
+          p0 = v0 ? p0 : 0.f;
+          p1 = v1 ? p1 : 0.f;
+        }
+        gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + nd),
+                                p1 * (__uint_as_float(dr[e + 1]) + nd));
+      }
+      // packed dS over the first 16 of the 32 columns this thread just read
+      tmem_st16(s_addr, gk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DQB_PFULL + x));
+    }
+    if (ok && wait(DQB_DONE, 0)) {
+      tc_fence_after();
+      __nv_bfloat16* out = dQ + (static_cast<size_t>(bh) * N + q) * HD + 64 * sub;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + DQ_TM_DQ + 64 * sub + 32 * c, r);
+        if (row_valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
+                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
+                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
+                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * scale, __uint_as_float(r[8 * i + 7]) * scale));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 size_t padded_len(int N) { return (static_cast<size_t>(N) + PAD - 1) / PAD * PAD; }
 
 template <class K>
-cudaError_t set_smem(K kernel) {
+cudaError_t set_smem(K kernel, uint32_t bytes = SMEM_BYTES) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(SMEM_BYTES));
+                              static_cast<int>(bytes));
 }
 
 }  // namespace
@@ -575,15 +846,19 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
                                  const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H,
                                  int Hkv, int N, float scale, int causal, int window,
-                                 const float* alibi, void* ws, cudaStream_t stream,
-                                 const TimingEvents& ev) {
+                                 const float* alibi, const BwdMaps* dq_maps, void* ws,
+                                 cudaStream_t stream, const TimingEvents& ev) {
   (void)q;
   (void)k;
   (void)v;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = set_smem(bwd_main_kernel<false>);
-    if (e == cudaSuccess) e = set_smem(bwd_main_kernel<true>);
+    cudaError_t e = set_smem(bwd_main_kernel<false, true>);
+    if (e == cudaSuccess) e = set_smem(bwd_main_kernel<true, true>);
+    if (e == cudaSuccess) e = set_smem(bwd_main_kernel<false, false>);
+    if (e == cudaSuccess) e = set_smem(bwd_main_kernel<true, false>);
+    if (e == cudaSuccess) e = set_smem(bwd_dq_kernel<false>, DQ_SMEM);
+    if (e == cudaSuccess) e = set_smem(bwd_dq_kernel<true>, DQ_SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -596,16 +871,19 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
                                           align256(rows * HD * sizeof(float)));
   float* lse_pad = reinterpret_cast<float*>(reinterpret_cast<char*>(d_pad) +
                                             align256(prows * sizeof(float)));
+  const bool deterministic = dq_maps != nullptr;
   bwd_pre_kernel<<<dim3(static_cast<unsigned>((prows + 15) / 16)), dim3(256), 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, d_pad,
-      lse_pad, dq_acc, N, Npad, prows);
+      lse_pad, deterministic ? nullptr : dq_acc, N, Npad, prows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int nkv = (N + BKV - 1) / BKV;
   if (ev.before) cudaEventRecord(ev.before, stream);
   const int g = H / Hkv;
   const int head_group = max(1, kHeadGroup / g);   // about kHeadGroup query heads in flight
-  auto kernel = alibi ? bwd_main_kernel<true> : bwd_main_kernel<false>;
+  auto kernel = deterministic
+                    ? (alibi ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>)
+                    : (alibi ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>);
   kernel<<<dim3(nkv * B * Hkv), dim3(NTHREADS), SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.dO, lse_pad, d_pad, dq_acc, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), B * Hkv, N, Npad, scale, causal, g, window, head_group,
@@ -613,6 +891,15 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;
+  if (deterministic) {
+    // dQ by query blocks, in a fixed key order, written once (no atomics)
+    const int npb = (N + DQ_BQ - 1) / DQ_BQ;
+    auto dqk = alibi ? bwd_dq_kernel<true> : bwd_dq_kernel<false>;
+    dqk<<<dim3(npb * BH), dim3(DQ_THREADS), DQ_SMEM, stream>>>(
+        dq_maps->q, dq_maps->k, dq_maps->v, dq_maps->dO, lse_pad, d_pad,
+        static_cast<__nv_bfloat16*>(dq), BH, N, Npad, scale, causal, g, window, alibi, H);
+    return cudaGetLastError();
+  }
   const size_t n8 = rows * HD / 8;
   bwd_convert_kernel<<<dim3(static_cast<unsigned>((n8 + 255) / 256)), dim3(256), 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), n8);

@@ -95,8 +95,8 @@ def main():
             _lib.check(_lib.fa_backward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                             o.data_ptr(), lse.data_ptr(), do.data_ptr(),
                                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq,
-                                            Hkv, N, d, scale, 1, 0, None, ws.data_ptr(), nbytes,
-                                            sh))
+                                            Hkv, N, d, scale, 1, 0, None, 0, ws.data_ptr(),
+                                            nbytes, sh))
     elif a.case == "dec_gqa":
         B, Hq, Hkv, L, S = 4, 32, 8, 32768, 8
         q, kc, vc = inputs.decode_gqa_inputs(B, Hq, Hkv, L, d, torch.bfloat16, 7, dev)

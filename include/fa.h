@@ -192,11 +192,19 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
 /*
  * fa_backward_gqa -- fa_backward with grouped query heads, an optional
  * causal sliding window and optional ALiBi slopes (same meaning as in
- * fa_forward_gqa; the slopes must match the forward call's).  dK and dV of a
+ * fa_forward_gqa; the slopes must match the forward call's), and an
+ * optional deterministic dQ.  dK and dV of a
  * key/value head are the sums of the gradients of its g query heads.
  *
  *   q, o, dO, dq  [B,Hq,N,d] bf16;  k, v, dk, dv [B,Hkv,N,d] bf16;
  *   lse           [B,Hq,N] fp32 from fa_forward_gqa with the same arguments.
+ *   deterministic 0: dQ is summed over key blocks with fp32 atomics (fast;
+ *                 summation order varies from run to run).  1: dK and dV
+ *                 come from one kernel and dQ from a second one that walks
+ *                 the key blocks of each 128-query block in a fixed order
+ *                 and writes dQ once; dQ, dK and dV are then bitwise
+ *                 reproducible (about 40% more work: S and dP are computed
+ *                 twice).  Other values: FA_ERR_INVALID_ARG.
  *   ws            NULL: the workspace comes from the library pool as in
  *                 fa_backward; otherwise a caller-owned device buffer of
  *                 ws_bytes >= fa_workspace_size(FA_OP_BACKWARD, B, Hq, N, d, 0)
@@ -206,8 +214,8 @@ int fa_backward_ex(const void* q, const void* k, const void* v, const void* o,
 int fa_backward_gqa(const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                    int window, const float* alibi_slopes, void* ws, size_t ws_bytes,
-                    cudaStream_t stream);
+                    int window, const float* alibi_slopes, int deterministic, void* ws,
+                    size_t ws_bytes, cudaStream_t stream);
 
 /*
  * fa_decode -- split-KV attention of one new query token per sequence over

@@ -93,9 +93,9 @@ def test_gqa_window_validation(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 64, 0.1, 1, 4, None, None) == E.FA_ERR_UNSUPPORTED
     args = [FAKE] * 9
     b = E.fa_backward_gqa
-    assert b(*args, 1, 4, 3, 8, 128, 0.1, 1, 0, None, None, 0, None) == E.FA_ERR_INVALID_ARG
-    assert b(*args, 1, 4, 2, 8, 128, 0.1, 0, 2, None, None, 0, None) == E.FA_ERR_UNSUPPORTED
-    assert b(*args, 1, 4, 2, 8, 128, 0.1, 1, 2, None, FAKE, 16, None) == E.FA_ERR_INVALID_ARG
+    assert b(*args, 1, 4, 3, 8, 128, 0.1, 1, 0, None, 0, None, 0, None) == E.FA_ERR_INVALID_ARG
+    assert b(*args, 1, 4, 2, 8, 128, 0.1, 0, 2, None, 0, None, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert b(*args, 1, 4, 2, 8, 128, 0.1, 1, 2, None, 0, FAKE, 16, None) == E.FA_ERR_INVALID_ARG
     assert "workspace" in E.fa_last_error()
     # misaligned slopes
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 8, 128, 0.1, 1, 0, MIS, None) == E.FA_ERR_INVALID_ARG
