@@ -548,7 +548,7 @@ def measure_targets(args, dev, peaks, peak_src):
                          dtype=torch.uint8, device=dev)
         ms = time_kernel(lambda: _lib.check(_lib.fa_decode_gqa(
             q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, w.B, w.H, hkv, w.N,
-            w.d, s, 1 / math.sqrt(w.d), ws.data_ptr(), ws.numel(), sh)), False)
+            w.d, s, 1 / math.sqrt(w.d), None, ws.data_ptr(), ws.numel(), sh)), False)
         gbs = kv_bytes / (ms * 1e-3) / 1e9
         rec = {"num_splits": s, "ms": round(ms, 4), "kv_gbs": round(gbs, 1),
                "frac": round(gbs / hbm, 4)}

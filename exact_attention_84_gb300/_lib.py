@@ -36,7 +36,7 @@ SIGNATURES = {
                             _P, _P, _Z, _P]),
     "fa_backward_gqa": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I,
                              _I, _P, _I, _P, _Z, _P]),
-    "fa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P]),
+    "fa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _Z, _P]),
     "fa_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_backward_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I,
                             _P, _Z, _P]),
@@ -110,10 +110,10 @@ def fa_backward_gqa(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, scale, ca
                  causal, window, alibi_slopes, deterministic, ws, ws_bytes, stream)
 
 
-def fa_decode_gqa(q, kcache, vcache, o, lse_out, B, Hq, Hkv, Lkv, d, num_splits, scale, ws,
-                  ws_bytes, stream):
+def fa_decode_gqa(q, kcache, vcache, o, lse_out, B, Hq, Hkv, Lkv, d, num_splits, scale,
+                  alibi_slopes, ws, ws_bytes, stream):
     return _call("fa_decode_gqa", q, kcache, vcache, o, lse_out, B, Hq, Hkv, Lkv, d, num_splits,
-                 scale, ws, ws_bytes, stream)
+                 scale, alibi_slopes, ws, ws_bytes, stream)
 
 
 def fa_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, stream):

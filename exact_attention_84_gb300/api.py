@@ -121,24 +121,25 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
 
 
 def decode(q, kcache, vcache, num_splits: int = 1, scale: float | None = None,
-           with_lse: bool = False, workspace=None):
+           with_lse: bool = False, workspace=None, alibi_slopes=None):
     """o (and optionally lse) for one query token per (b, h): q [B, H, d],
     caches [B, Hkv, Lkv, d], all bf16 (H a multiple of Hkv: query head h
-    reads cache head h // (H // Hkv))."""
+    reads cache head h // (H // Hkv)).  ``alibi_slopes``: H fp32 slopes; the
+    new token is at position Lkv - 1."""
     B, Hkv, L, d = kcache.shape
     H = q.shape[1]
     for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
         _need(t, torch.bfloat16, n)
     o = torch.empty_like(q)
     lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if with_lse else None
-    if Hkv != H:
+    if Hkv != H or alibi_slopes is not None:
         scale = 1.0 / math.sqrt(d) if scale is None else scale
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
         _lib.check(_lib.fa_decode_gqa(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
                                       o.data_ptr(), lse.data_ptr() if lse is not None else None,
-                                      B, H, Hkv, L, d, num_splits, scale, ws_ptr, ws_bytes,
-                                      _stream()))
+                                      B, H, Hkv, L, d, num_splits, scale,
+                                      _slopes(alibi_slopes, H), ws_ptr, ws_bytes, _stream()))
     elif scale is None and not with_lse and workspace is None:
         _lib.check(_lib.fa_decode(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
                                   o.data_ptr(), B, H, L, d, num_splits, _stream()))

@@ -381,7 +381,8 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
 
 int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o,
                   float* lse_out, int B, int Hq, int Hkv, int Lkv, int d, int num_splits,
-                  float scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                  float scale, const float* alibi_slopes, void* ws, size_t ws_bytes,
+                  cudaStream_t stream) {
   const char* fn = "fa_decode_gqa";
   if (!q || !kcache || !vcache || !o) return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (int r = check_sizes(B, Hq, Lkv, d)) return r;
@@ -396,7 +397,8 @@ int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o
       static_cast<long long>(B) * Hq > 65535ll)
     return fail(FA_ERR_UNSUPPORTED, "%s: B*Hq must be <= 65535", fn);
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
-      (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)))
+      (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) ||
+      (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
     return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
   const size_t need = fa::decode_workspace_bytes(B, Hq, num_splits);
   const bool own = (ws == nullptr);
@@ -415,9 +417,10 @@ int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o
   // One query head per key/value head is plain decode (per-row kernel).
   cudaError_t e = group == 1
                       ? fa::launch_decode(q, kcache, vcache, o, lse_out, B, Hq, Lkv, num_splits,
-                                          scale, ws, stream, g_events)
+                                          scale, ws, stream, g_events, alibi_slopes)
                       : fa::launch_decode_gqa(tk, tv, q, o, lse_out, B, Hq, Hkv, Lkv,
-                                              num_splits, scale, ws, stream, g_events);
+                                              num_splits, scale, ws, stream, g_events,
+                                              alibi_slopes);
   if (own) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess) e = e2;

@@ -23,6 +23,10 @@
 // for the 5th-generation tensor cores (64 rows at least) but a natural fit
 // for warp-level m16n8k16 MMAs with fp32 accumulation, which keep S, P and
 // the output in registers.  The kernel stays bound by the cache read.
+//
+// ALiBi ("03. FlashAttention", "Variantes et extensions": the linear bias
+// fused into the kernel): the new token sits at position L - 1, after every
+// cached row, so row j of head h gets -slope_h (L - 1 - j) on its score.
 #include <cfloat>
 #include <mutex>
 
@@ -67,7 +71,8 @@ __device__ __forceinline__ void bf16x4_to_float(uint2 u, float* f) {
 __global__ void __launch_bounds__(NTHREADS, 2)
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
                     const __nv_bfloat16* __restrict__ vc, float* __restrict__ part_o,
-                    float* __restrict__ part_lse, int L, int S, int chunk, float scale_log2) {
+                    float* __restrict__ part_lse, int L, int S, int chunk, float scale_log2,
+                    const float* __restrict__ alibi, int heads) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -124,6 +129,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     }
     float m = -INFINITY, l = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float slope_log2 = alibi != nullptr ? alibi[bh % heads] * 1.4426950408889634f : 0.f;
     for (int t = 0; t < nchunks; ++t) {
       const int st = t % STAGES;
       if (!mbar_wait(sbase + OFF_BAR + 8 * st, (t / STAGES) & 1, abort_flag, &g_status_decode))
@@ -149,7 +155,10 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 #pragma unroll
       for (int i = 0; i < ROWS_PER_WARP; ++i) {
         sc[i] = warp_sum(sc[i]);
-        if (warp * ROWS_PER_WARP + i >= rows) sc[i] = -INFINITY;
+        const int r = warp * ROWS_PER_WARP + i;
+        if (alibi != nullptr)   // ALiBi: -slope (L - 1 - j) in log2 units
+          sc[i] = fmaf(-slope_log2, static_cast<float>(L - 1 - (r0 + t * ROWS + r)), sc[i]);
+        if (r >= rows) sc[i] = -INFINITY;
       }
       float mx = sc[0];
 #pragma unroll
@@ -280,7 +289,8 @@ decode_gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
                         const __nv_bfloat16* __restrict__ q, float* __restrict__ part_o,
                         float* __restrict__ part_lse, int L, int S, int chunk, int group,
-                        int nslice, float scale_log2) {
+                        int nslice, float scale_log2, const float* __restrict__ alibi,
+                        int heads) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -360,6 +370,9 @@ decode_gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     const int mi = lane >> 3, mr = lane & 7;        // ldmatrix: matrix index, row in it
+    // ALiBi slopes of rows gid and gid + 8 (log2 units; 0 without ALiBi)
+    const float slope0 = (alibi != nullptr && gid < nh) ? alibi[(h0 + gid) % heads] * 1.4426950408889634f : 0.f;
+    const float slope1 = (alibi != nullptr && gid + 8 < nh) ? alibi[(h0 + gid + 8) % heads] * 1.4426950408889634f : 0.f;
     for (int t = 0; t < nst; ++t) {
       const int st = t % G_STAGES;
       if (!mbar_wait(full_bar(st), (t / G_STAGES) & 1, abort_flag, &g_status_decode)) break;
@@ -377,14 +390,16 @@ decode_gqa_split_kernel(const __grid_constant__ CUtensorMap tmK,
           mma16816(sc[1], qa[k][0], qa[k][1], qa[k][2], qa[k][3], b2, b3);
         }
       }
-      // keys of this stage past the split (or the cache) are masked
+      // keys of this stage past the split (or the cache) are masked; ALiBi
+      // adds -slope (L - 1 - j) (rows gid and gid + 8 have their own slopes)
       const int kbase = r0 + t * G_ROWS + 16 * warp + 2 * tig;
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = kbase + 8 * n + (e & 1);
-          sc[n][e] = key < r_end ? sc[n][e] * scale_log2 : -INFINITY;
+          const float bias = -(e < 2 ? slope0 : slope1) * static_cast<float>(L - 1 - key);
+          sc[n][e] = key < r_end ? fmaf(sc[n][e], scale_log2, bias) : -INFINITY;
         }
       float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
       float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -491,7 +506,8 @@ size_t decode_workspace_bytes(int B, int H, int num_splits) {
 
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o,
                           float* lse_out, int B, int H, int L, int num_splits, float scale,
-                          void* ws, cudaStream_t stream, const TimingEvents& ev) {
+                          void* ws, cudaStream_t stream, const TimingEvents& ev,
+                          const float* alibi) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
@@ -510,7 +526,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
   decode_split_kernel<<<dim3(num_splits, BH), dim3(NTHREADS), SMEM_BYTES, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
       static_cast<const __nv_bfloat16*>(vc), part_o, part_lse, L, num_splits, chunk,
-      scale * 1.4426950408889634f);
+      scale * 1.4426950408889634f, alibi, H);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;
@@ -522,7 +538,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
 cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q,
                               void* o, float* lse_out, int B, int Hq, int Hkv, int L,
                               int num_splits, float scale, void* ws, cudaStream_t stream,
-                              const TimingEvents& ev) {
+                              const TimingEvents& ev, const float* alibi) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(decode_gqa_split_kernel,
@@ -542,7 +558,7 @@ cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, co
   decode_gqa_split_kernel<<<dim3(num_splits, B * Hkv * nslice), dim3(G_THREADS), G_SMEM,
                             stream>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(q), part_o,
                                       part_lse, L, num_splits, chunk, group, nslice,
-                                      scale * 1.4426950408889634f);
+                                      scale * 1.4426950408889634f, alibi, Hq);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;

@@ -65,16 +65,19 @@ int status_backward_bf16(bool clear);
 
 // ---- split-KV decode (decode.cu)
 size_t decode_workspace_bytes(int B, int H, int num_splits);
+// alibi: nullptr, or H (query-head) ALiBi slopes: row j of the cache gets
+// -slope (L - 1 - j) on its score.
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o,
                           float* lse_out, int B, int H, int L, int num_splits, float scale,
-                          void* ws, cudaStream_t stream, const TimingEvents& ev);
+                          void* ws, cudaStream_t stream, const TimingEvents& ev,
+                          const float* alibi = nullptr);
 int status_decode(bool clear);
 // Grouped heads (Hq = g * Hkv): tensor maps over the caches [B*Hkv, L, 128]
 // with 64-row boxes; partials and workspace as launch_decode with H = Hq.
 cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q,
                               void* o, float* lse_out, int B, int Hq, int Hkv, int L,
                               int num_splits, float scale, void* ws, cudaStream_t stream,
-                              const TimingEvents& ev);
+                              const TimingEvents& ev, const float* alibi = nullptr);
 
 // Fixed device scratch of fa_decode_noalloc (decode.cu): room for
 // kNoAllocMaxParts = B * H * num_splits partial results.

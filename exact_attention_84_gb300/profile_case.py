@@ -106,8 +106,8 @@ def main():
 
         def call():
             _lib.check(_lib.fa_decode_gqa(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
-                                          None, B, Hq, Hkv, L, d, S, scale, ws.data_ptr(), nbytes,
-                                          sh))
+                                          None, B, Hq, Hkv, L, d, S, scale, None, ws.data_ptr(),
+                                          nbytes, sh))
     else:
         B, H, L, S = 4, 32, 32768, 8
         q, kc, vc = inputs.decode_inputs(B, H, L, d, torch.bfloat16, 4, dev)

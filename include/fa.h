@@ -259,14 +259,18 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
  *
  *   q, o      [B,Hq,d] bf16;  kcache, vcache [B,Hkv,Lkv,d] bf16;
  *   lse_out   [B,Hq] fp32 or NULL.
+ *   alibi_slopes  NULL, or a DEVICE array of Hq fp32 slopes: the new token
+ *             sits at position Lkv - 1, so cache row j of query head h gets
+ *             -slope_h * (Lkv - 1 - j) on its score (ALiBi, as in
+ *             fa_forward_gqa).
  *   Hkv >= 1, Hq % Hkv == 0, B*Hq <= 65535.  Splits, scale and workspace as
  *   in fa_decode_ex, with the workspace sized by
  *   fa_workspace_size(FA_OP_DECODE, B, Hq, Lkv, d, num_splits).
  */
 int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o,
                   float* lse_out, int B, int Hq, int Hkv, int Lkv, int d,
-                  int num_splits, float scale, void* ws, size_t ws_bytes,
-                  cudaStream_t stream);
+                  int num_splits, float scale, const float* alibi_slopes, void* ws,
+                  size_t ws_bytes, cudaStream_t stream);
 
 /*
  * fa_decode_noalloc -- fa_decode_ex without any allocation.  The pages have

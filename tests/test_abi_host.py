@@ -108,10 +108,10 @@ def test_gqa_window_validation(lib):
     assert p8(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 8, 128, 0.1, 1.0, 1.0, 1.0, 1, 0, None, FAKE, 8,
               None) == E.FA_ERR_INVALID_ARG
     d = E.fa_decode_gqa
-    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 3, 100, 128, 2, 0.1, None, 0, None) == E.FA_ERR_INVALID_ARG
-    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 0, 0.1, None, 0, None) == E.FA_ERR_INVALID_ARG
-    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, FAKE, 8, None) == E.FA_ERR_INVALID_ARG
-    assert d(FAKE, None, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, 0, None) == E.FA_ERR_INVALID_ARG
+    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 3, 100, 128, 2, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
+    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 0, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
+    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, FAKE, 8, None) == E.FA_ERR_INVALID_ARG
+    assert d(FAKE, None, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
 
 
 def test_workspace_sizes(lib):

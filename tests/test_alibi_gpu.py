@@ -114,3 +114,19 @@ def test_alibi_long_causal_n8192_sampled():
                                                     np64(v[0, h]), rows, SCALE, True,
                                                     slope=float(sl[h]))
         assert_close_bf16(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, f"head {h}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L", [(2, 4, 4, 1000), (1, 8, 2, 513), (2, 32, 1, 300),
+                                        (1, 2, 2, 1)])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_alibi_decode(B, Hq, Hkv, L, splits):
+    """Decode with ALiBi: the new token at position L - 1 (both decode
+    kernels: one query head per cache head, and grouped heads)."""
+    if splits > L:
+        pytest.skip("num_splits > Lkv is rejected by the API")
+    q, kc, vc = inputs.decode_gqa_inputs(B, Hq, Hkv, L, D, torch.bfloat16, 130 + L, "cuda")
+    slopes = inputs.alibi_slopes(Hq, "cuda")
+    o, lse = api.decode(q, kc, vc, num_splits=splits, scale=SCALE, with_lse=True,
+                        alibi_slopes=slopes)
+    o_ref, lse_ref = orc.attention_decode_gqa(np64(q), np64(kc), np64(vc), SCALE, np64(slopes))
+    assert_close_bf16(o, lse, o_ref, lse_ref, f"L={L} g={Hq // Hkv} splits={splits}")

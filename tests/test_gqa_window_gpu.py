@@ -98,7 +98,7 @@ def test_decode_gqa(B, Hq, Hkv, L, splits):
     ws = torch.empty(_lib.fa_workspace_size(_lib.FA_OP_DECODE, B, Hq, L, D, splits),
                      dtype=torch.uint8, device="cuda")
     _lib.check(_lib.fa_decode_gqa(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o_view.data_ptr(),
-                                  None, B, Hq, Hkv, L, D, splits, SCALE, ws.data_ptr(),
+                                  None, B, Hq, Hkv, L, D, splits, SCALE, None, ws.data_ptr(),
                                   ws.numel(), torch.cuda.current_stream().cuda_stream))
     assert torch.equal(o_view, o)
     assert guards_intact(bo)
