@@ -294,13 +294,13 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
   if (deterministic != 0 && deterministic != 1)
     return fail(FA_ERR_INVALID_ARG, "%s: deterministic must be 0 or 1", fn);
   fa::BwdMaps maps, dq_maps;
-  if (int r = make_map(&maps.q, q, B * Hq, N, 128)) return r;    // 128-query blocks
-  if (int r = make_map(&maps.dO, dO, B * Hq, N, 128)) return r;
+  if (int r = make_map(&maps.q, q, B * Hq, N, 64)) return r;     // 64-query blocks
+  if (int r = make_map(&maps.dO, dO, B * Hq, N, 64)) return r;
   if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
-  if (deterministic) {                                            // 64-key tiles
-    dq_maps.q = maps.q;
-    dq_maps.dO = maps.dO;
+  if (deterministic) {                                            // 128-query blocks, 64-key tiles
+    if (int r = make_map(&dq_maps.q, q, B * Hq, N, 128)) return r;
+    if (int r = make_map(&dq_maps.dO, dO, B * Hq, N, 128)) return r;
     if (int r = make_map(&dq_maps.k, k, B * Hkv, N, 64)) return r;
     if (int r = make_map(&dq_maps.v, v, B * Hkv, N, 64)) return r;
   }

@@ -14,26 +14,23 @@
 //                to a multiple of 128 rows (so every block copy is aligned
 //                and in bounds), and zeroing of the fp32 dQ accumulator.
 //   bwd_main     one thread block per (b, h, 128-key block j).  K_j and V_j
-//                stay in shared memory; 128-row blocks Q_i, dO_i (with their
-//                LSE and D) stream past in a 2-stage TMA ring.  Per block i:
-//                  S^T  = K_j Q_i^T   -> R0   (shared-memory operands)
-//                  dP^T = V_j dO_i^T  -> R1
+//                stay in shared memory; 64-row blocks Q_i, dO_i (with their
+//                LSE and D) stream past in a 3-stage TMA ring.  Per block i,
+//                in one of two TMEM buffers X = i mod 2:
+//                  S^T  = K_j Q_i^T   -> R0_X   (shared-memory operands)
+//                  dP^T = V_j dO_i^T  -> R1_X
 //                  softmax warps (key row = TMEM lane) form
 //                  P^T = exp2(S^T scale log2e - LSE log2e) and
 //                  dS^T = P^T (dP^T - D), write both as packed bf16 over the
-//                  R0 columns they were computed from, and dS^T also to
-//                  shared memory;
-//                  dQ_i^T = K_j^T dS^T -> R1      (both operands MN-major)
+//                  R0_X columns they were computed from, and dS^T also to
+//                  shared memory (double-buffered);
+//                  dQ_i^T = K_j^T dS^T -> R1_X    (both operands MN-major)
 //                  dV += P^T dO_i, dK += dS^T Q_i  (A operand from TMEM)
-//                Every product is 128 x 128: the 5th-generation tensor cores
-//                run those at full rate, while 128 x 64 products (64-query
-//                blocks, which would leave room to double-buffer S^T / dP^T)
-//                measured at half the rate per FLOP.  TMEM holds exactly R0,
-//                R1, dV and dK (4 x 128 columns).  Four writer warps add
-//                scale * dQ_i into the fp32 accumulator with 16-byte vector
-//                atomics after a 4x4 register transpose (one warp instruction
-//                covers 4 rows x 128 contiguous bytes) while dV and dK are
-//                formed.  dK and dV leave TMEM once.
+//                Block i's softmax overlaps the products of blocks i-1 and
+//                i+1; four writer warps add scale * dQ_i into the fp32
+//                accumulator with 16-byte vector atomics after a 4x4 register
+//                transpose (one warp instruction covers 4 rows x 128
+//                contiguous bytes).  dK and dV leave TMEM once.
 //   bwd_convert  dQ = bf16(accumulator).
 // Causal: query blocks entirely above the key block are skipped; the blocks
 // that straddle the diagonal are masked element-wise.
@@ -58,38 +55,38 @@ __device__ int g_status_bwd;
 
 constexpr int HD = 128;
 constexpr int BKV = 128;                  // key rows per block (TMEM lanes)
-constexpr int BQ = 128;                   // query rows per streamed block
+constexpr int BQ = 64;                    // query rows per streamed block
 constexpr int PAD = 128;                  // per-head padding of the staged LSE / D
-constexpr int STAGES = 2;
-constexpr uint32_t TILE = 128 * HD * 2;   // K_j, V_j, Q_i or dO_i: 32 KiB
+constexpr int STAGES = 3;
+constexpr uint32_t TILE = 128 * HD * 2;   // K_j or V_j: 32 KiB
 constexpr uint32_t HALF = TILE / 2;       // 128 rows x 64 columns
-constexpr uint32_t STAT = BQ * 4;         // 512 B of -LSE*log2e or -D per block
-constexpr uint32_t DS_TILE = BKV * BQ * 2;   // dS^T [key][query]: 32 KiB
-constexpr uint32_t DS_HALF = DS_TILE / 2;    // 128 keys x 64 queries
+constexpr uint32_t QTILE = BQ * HD * 2;   // Q_i or dO_i: 16 KiB
+constexpr uint32_t QHALF = QTILE / 2;     // 64 rows x 64 columns
+constexpr uint32_t STAT = BQ * 4;         // 256 B of -LSE*log2e or -D per block
+constexpr uint32_t DS_TILE = BKV * BQ * 2;                   // dS^T [key][query]: 16 KiB
 
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + TILE;
 constexpr uint32_t OFF_STAGE = OFF_V + TILE;
-constexpr uint32_t ST_Q = 0, ST_DO = TILE, ST_LSE = 2 * TILE, ST_D = 2 * TILE + STAT;
-constexpr uint32_t STAGE_BYTES = 2 * TILE + 1024;              // 1024-aligned stages
-constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_DS + DS_TILE;
+constexpr uint32_t ST_Q = 0, ST_DO = QTILE, ST_LSE = 2 * QTILE, ST_D = 2 * QTILE + STAT;
+constexpr uint32_t STAGE_BYTES = 2 * QTILE + 2048;           // 1024-aligned stages
+constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES; // 2 buffers
+constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_TILE;
 constexpr int B_KVFULL = 0;
 constexpr int B_QFULL = 1;                 // + stage
 constexpr int B_QEMPTY = B_QFULL + STAGES; // + stage
-constexpr int B_SFULL = B_QEMPTY + STAGES; // S^T and dP^T in TMEM
-constexpr int B_PFULL = B_SFULL + 1;       // P^T, dS^T written (8 warps)
-constexpr int B_DQFULL = B_PFULL + 1;      // dQ^T in TMEM
-constexpr int B_DQFREE = B_DQFULL + 1;     // 4 writer warps have read dQ^T
-constexpr int B_DONE = B_DQFREE + 1;       // every product of the block completed
+constexpr int B_SFULL = B_QEMPTY + STAGES; // + buffer: S^T and dP^T in TMEM
+constexpr int B_PFULL = B_SFULL + 2;       // + buffer: P^T, dS^T written (8 warps)
+constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
+constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
+constexpr int B_DONE = B_DQFREE + 2;       // every product of the block completed
 constexpr int NBAR = B_DONE + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // base is 1024-aligned (checked)
-static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
 constexpr uint32_t TMEM_COLS = 512;
-// R0: S^T, then P^T | dS^T packed; R1: dP^T, then dQ^T; dV; dK
-constexpr uint32_t TM_R0 = 0, TM_R1 = 128, TM_DV = 256, TM_DK = 384;
+// buffer X: R0 = [128 X, 128 X + 64), R1 = [128 X + 64, 128 X + 128)
+constexpr uint32_t TM_DV = 256, TM_DK = 384;
 
 constexpr int NTHREADS = 448;   // 0-7 softmax, 8-11 dQ writers, 12 producer, 13 MMA
 constexpr int WARP_TMA = 12;
@@ -97,11 +94,11 @@ constexpr int WARP_MMA = 13;
 constexpr int kHeadGroup = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 128 queries.
+// S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 64 queries.
 constexpr uint32_t IDESC_ST = idesc_bf16(BKV, BQ, false, false);
 // dV += P^T dO_i, dK += dS^T Q_i: A in TMEM, B MN-major; M = 128 keys, N = d.
 constexpr uint32_t IDESC_DKV = idesc_bf16(BKV, HD, false, true);
-// dQ_i^T = K_j^T dS^T: M = d, N = 128 queries; both operands MN-major.
+// dQ_i^T = K_j^T dS^T: M = d, N = 64 queries; both operands MN-major.
 constexpr uint32_t IDESC_DQ = idesc_bf16(HD, BQ, true, true);
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
@@ -253,10 +250,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_QFULL + s), 1);
       mbar_init(bar_addr(sbase, B_QEMPTY + s), 1);
     }
-    mbar_init(bar_addr(sbase, B_SFULL), 1);
-    mbar_init(bar_addr(sbase, B_PFULL), 8);
-    mbar_init(bar_addr(sbase, B_DQFULL), 1);
-    mbar_init(bar_addr(sbase, B_DQFREE), 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar_addr(sbase, B_SFULL + x), 1);
+      mbar_init(bar_addr(sbase, B_PFULL + x), 8);
+      mbar_init(bar_addr(sbase, B_DQFULL + x), 1);
+      mbar_init(bar_addr(sbase, B_DQFREE + x), 4);
+    }
     mbar_init(bar_addr(sbase, B_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -291,11 +290,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (it >= STAGES && !ctx.wait(B_QEMPTY + st, ((it / STAGES) - 1) & 1)) break;
         const uint32_t qf = bar_addr(sbase, B_QFULL + st);
         const uint32_t sb = sbase + OFF_STAGE + st * STAGE_BYTES;
-        mbar_arrive_expect_tx(qf, 2 * TILE + 2 * STAT);
+        mbar_arrive_expect_tx(qf, 2 * QTILE + 2 * STAT);
         tma_load_3d(sb + ST_Q, &tmQ, qf, 0, qb, bh);
-        tma_load_3d(sb + ST_Q + HALF, &tmQ, qf, 64, qb, bh);
+        tma_load_3d(sb + ST_Q + QHALF, &tmQ, qf, 64, qb, bh);
         tma_load_3d(sb + ST_DO, &tmdO, qf, 0, qb, bh);
-        tma_load_3d(sb + ST_DO + HALF, &tmdO, qf, 64, qb, bh);
+        tma_load_3d(sb + ST_DO + QHALF, &tmdO, qf, 64, qb, bh);
         const size_t srow = static_cast<size_t>(bh) * Npad + qb;
         bulk_load(sb + ST_LSE, lse_pad + srow, STAT, qf);
         bulk_load(sb + ST_D, d_pad + srow, STAT, qf);
@@ -304,19 +303,20 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    // Order, per query block i:
-    //   [P(i) ready] dQ^T(i) dV(i) dK(i) | S^T(i+1) [dQ^T(i) drained] dP^T(i+1)
-    // so the writers drain dQ^T(i) while dV(i), dK(i) and S^T(i+1) run.
+    // Order, per query block i in buffer X = i mod 2:
+    //   [P(i) ready] dQ^T(i) dV(i) dK(i) | S^T(i+2) [dQ^T(i) drained] dP^T(i+2)
+    // so block i+1's softmax overlaps block i's gradient products and block
+    // i+2's score products, and the writers drain dQ^T(i) meanwhile.
     if (lane == 0) {
       const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V;
       auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
-      const uint32_t r0 = tmem + TM_R0, r1 = tmem + TM_R1;
+      auto r0 = [&](int it) { return tmem + 128u * (it & 1); };
+      auto r1 = [&](int it) { return tmem + 128u * (it & 1) + 64u; };
       // Descriptors of the key-block operands, fixed for the whole block; a
       // k-step advances the start-address field (units of 16 bytes).
       const uint64_t kd_k = sdesc_sw128(kA, 16, 1024);        // K_j, K-major (S^T)
       const uint64_t vd_k = sdesc_sw128(vA, 16, 1024);        // V_j, K-major (dP^T)
       const uint64_t kd_mn = sdesc_sw128(kA, HALF, 1024);     // K_j^T, MN-major (dQ^T)
-      const uint64_t dsd = sdesc_sw128(sbase + OFF_DS, DS_HALF, 1024);   // dS^T, MN-major
       // S^T (into R0) or dP^T (into R1): reduction over d.
       auto issue_sdp = [&](int it, bool dp) {
         const uint64_t ad = dp ? vd_k : kd_k;
@@ -324,69 +324,71 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint64_t a[8], b[8];
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t off = ((kk >> 2) * HALF + (kk & 3) * 32) >> 4;
-          a[kk] = ad + off;
-          b[kk] = bd + off;
+          a[kk] = ad + (((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+          b[kk] = bd + (((kk >> 2) * QHALF + (kk & 3) * 32) >> 4);
         }
-        mma_ss_batch8(dp ? r1 : r0, a, b, IDESC_ST, 0u);
+        mma_ss_batch8(dp ? r1(it) : r0(it), a, b, IDESC_ST, 0u);
       };
       auto wait_q = [&](int it) {
         return ctx.wait(B_QFULL + it % STAGES, (it / STAGES) & 1);
       };
-      bool ok = ctx.wait(B_KVFULL, 0) && wait_q(0);
-      if (ok) {
+      bool ok = ctx.wait(B_KVFULL, 0);
+      for (int it = 0; it < 2 && it < nit && ok; ++it) {
+        if (!(ok = wait_q(it))) break;
         tc_fence_after();
-        issue_sdp(0, false);
-        issue_sdp(0, true);
-        mma_commit(bar_addr(sbase, B_SFULL));
+        issue_sdp(it, false);
+        issue_sdp(it, true);
+        mma_commit(bar_addr(sbase, B_SFULL + (it & 1)));
       }
       for (int it = 0; it < nit && ok; ++it) {
+        const int x = it & 1;
         const uint32_t sb = stage(it);
-        if (!(ok = ctx.wait(B_PFULL, it & 1))) break;
+        if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
         tc_fence_after();
-        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1.
+        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
         if constexpr (kDq) {
+          const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
           uint64_t a[8], b[8];
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
             a[kk] = kd_mn + ((kk * 2048) >> 4);
             b[kk] = dsd + ((kk * 2048) >> 4);
           }
-          mma_ss_batch8(r1, a, b, IDESC_DQ, 0u);
-          mma_commit(bar_addr(sbase, B_DQFULL));
+          mma_ss_batch8(r1(it), a, b, IDESC_DQ, 0u);
+          mma_commit(bar_addr(sbase, B_DQFULL + x));
         }
-        // dV += P^T dO_i, dK += dS^T Q_i.  R0 holds, per 32-query slice g,
+        // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
         // P^T packed in columns [32g, 32g+16) and dS^T in [32g+16, 32g+32);
         // 16 queries = 8 packed columns.
         {
-          const uint64_t dod = sdesc_sw128(sb + ST_DO, HALF, 1024);   // dO_i, MN-major
-          const uint64_t qd = sdesc_sw128(sb + ST_Q, HALF, 1024);     // Q_i, MN-major
-          uint32_t ap[8], as[8];
-          uint64_t bo[8], bq[8];
+          const uint64_t dod = sdesc_sw128(sb + ST_DO, QHALF, 1024);   // dO_i, MN-major
+          const uint64_t qd = sdesc_sw128(sb + ST_Q, QHALF, 1024);     // Q_i, MN-major
+          uint32_t ap[4], as[4];
+          uint64_t bo[4], bq[4];
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
-            ap[kk] = r0 + 32 * (kk >> 1) + 8 * (kk & 1);
+            ap[kk] = r0(it) + 32 * (kk >> 1) + 8 * (kk & 1);
             as[kk] = ap[kk] + 16;
             bo[kk] = dod + ((kk * 2048) >> 4);
             bq[kk] = qd + ((kk * 2048) >> 4);
           }
           const uint32_t acc = it > 0 ? 1u : 0u;
-          mma_ts_batch8(tmem + TM_DV, ap, bo, IDESC_DKV, acc);
-          mma_ts_batch8(tmem + TM_DK, as, bq, IDESC_DKV, acc);
+          mma_ts_batch4(tmem + TM_DV, ap, bo, IDESC_DKV, acc);
+          mma_ts_batch4(tmem + TM_DK, as, bq, IDESC_DKV, acc);
         }
         mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
-        if (it + 1 < nit) {
-          // R0 was read by dV/dK(i) (issued above, executed in order).
-          if (!(ok = wait_q(it + 1))) break;
+        if (it + 2 < nit) {
+          // R0_X was read by dV/dK(i) (issued above, executed in order).
+          if (!(ok = wait_q(it + 2))) break;
           tc_fence_after();
-          issue_sdp(it + 1, false);
-          // R1 holds dQ^T(i) until the writers have read it.
+          issue_sdp(it + 2, false);
+          // R1_X holds dQ^T(i) until the writers have read it.
           if constexpr (kDq) {
-            if (!(ok = ctx.wait(B_DQFREE, it & 1))) break;
+            if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
             tc_fence_after();
           }
-          issue_sdp(it + 1, true);
-          mma_commit(bar_addr(sbase, B_SFULL));
+          issue_sdp(it + 2, true);
+          mma_commit(bar_addr(sbase, B_SFULL + x));
         }
       }
       if (ok) mma_commit(bar_addr(sbase, B_DONE));
@@ -394,8 +396,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    // Warp w takes the rows of TMEM lane quadrant w & 3 and the 64-query
-    // half w >> 2 of each 128-query block, in two slices of 32.
+    // Warp w takes the rows of TMEM lane quadrant w & 3 and the 32-query
+    // slice w >> 2 of each 64-query block.
     const int sub = warp >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;                 // key row within block j
@@ -408,17 +410,20 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     bool ok = true;
     Cursor cur = first;
     for (int it = 0; it < nit; ++it, cur.next(i0, i1)) {
+      const int x = it & 1;
       const int st = it % STAGES;
       const int qb = cur.qi * BQ;
       const float slope_log2 = kAlibi ? alibi[cur.hq % heads] * kLog2e : 0.f;
+      const float d0 = static_cast<float>(qb + sub * 32 - kv);   // query - key at column 0
       const float* stage_lse =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_D);
       // QFULL: the staged LSE / D are visible here; SFULL: S^T, dP^T in TMEM.
-      // SFULL(i) is committed after dQ^T(i-1), the last reader of the dS^T
-      // shared buffer, so the buffer is free as well.
-      if (!ctx.wait(B_QFULL + st, (it / STAGES) & 1) || !ctx.wait(B_SFULL, it & 1)) {
+      // SFULL(i) is committed after dQ^T(i-2), the last reader of this
+      // block's dS^T shared buffer, so the buffer is free as well.
+      if (!ctx.wait(B_QFULL + st, (it / STAGES) & 1) ||
+          !ctx.wait(B_SFULL + x, (it >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -429,69 +434,64 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // ragged end need it; the test is block-uniform.
       const bool need_mask = (causal && qb < j * BKV + BKV) || (qb + BQ > N) ||
                              (j * BKV + BKV > N) || (window > 0 && qb + BQ > j * BKV + window);
-#pragma unroll 1
-      for (int sl = 0; sl < 2; ++sl) {
-        const int col0 = sub * 64 + sl * 32;            // first query column of this slice
-        const float d0 = static_cast<float>(qb + col0 - kv);   // query - key at column 0
-        const uint32_t s_addr = tmem + lane_addr + TM_R0 + col0;
-        uint32_t sr[32], dr[32];
-        tmem_ld32(s_addr, sr);
-        tmem_ld32(tmem + lane_addr + TM_R1 + col0, dr);
-        uint32_t pk[16], gk[16];
+      const int col0 = sub * 32;                      // first query column of this slice
+      const uint32_t s_addr = tmem + lane_addr + 128u * x + col0;
+      uint32_t sr[32], dr[32];
+      tmem_ld32(s_addr, sr);
+      tmem_ld32(s_addr + 64, dr);
+      uint32_t pk[16], gk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
-          float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
-          if constexpr (kAlibi) {
-            // exponent offset -LSE log2e - slope |i - j| log2e per query column
-            const float de = d0 + static_cast<float>(e);
-            l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
-            l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
-            l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
-            l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
-          }
-          float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
-          float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
-          float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
-          if (need_mask) {
-            // qlo <= q <= qhi as one unsigned compare per query (the
-            // wrap-around of rel + t is the exact difference mod 2^32)
-            const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
-            p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
-            p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
-            p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
-            p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
-          }
-          pk[e / 2] = pack_bf16x2(p0, p1);
-          pk[e / 2 + 1] = pack_bf16x2(p2, p3);
-          gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + d4.x),
-                                  p1 * (__uint_as_float(dr[e + 1]) + d4.y));
-          gk[e / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[e + 2]) + d4.z),
-                                      p3 * (__uint_as_float(dr[e + 3]) + d4.w));
+      for (int e = 0; e < 32; e += 4) {
+        // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
+        float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
+        const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
+        if constexpr (kAlibi) {
+          // exponent offset -LSE log2e - slope |i - j| log2e per query column
+          const float de = d0 + static_cast<float>(e);
+          l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
+          l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
+          l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
+          l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
         }
-        // Packed P^T and dS^T go over exactly the 32 columns this thread has
-        // just read (P^T first 16, dS^T last 16): no other warp reads them.
-        tmem_st16(s_addr, pk);
-        tmem_st16(s_addr + 16, gk);
-        // dS^T row into the shared buffer (MN-major operand of dQ^T): the
-        // 64-query box `sub`, 16-byte chunks 4 sl .. 4 sl + 3.
-        if constexpr (kDq) {
-          uint8_t* ds_smem = smem + OFF_DS + sub * DS_HALF;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const uint32_t off = sw128_offset(row, sl * 4 + ch);
-            *reinterpret_cast<uint4*>(ds_smem + off) =
-                make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
-          }
+        float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
+        float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
+        float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
+        float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
+        if (need_mask) {
+          // qlo <= q <= qhi as one unsigned compare per query (the
+          // wrap-around of rel + t is the exact difference mod 2^32)
+          const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
+          p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
+          p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
+          p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
+          p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
         }
+        pk[e / 2] = pack_bf16x2(p0, p1);
+        pk[e / 2 + 1] = pack_bf16x2(p2, p3);
+        gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + d4.x),
+                                p1 * (__uint_as_float(dr[e + 1]) + d4.y));
+        gk[e / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[e + 2]) + d4.z),
+                                    p3 * (__uint_as_float(dr[e + 3]) + d4.w));
       }
-      if constexpr (kDq) fence_proxy_async_smem();
+      // Packed P^T and dS^T go over exactly the 32 columns this thread has
+      // just read (P^T first 16, dS^T last 16): no other warp reads them.
+      tmem_st16(s_addr, pk);
+      tmem_st16(s_addr + 16, gk);
+      // dS^T row into this block's shared buffer (MN-major operand of dQ^T).
+      if constexpr (kDq) {
+        uint8_t* ds_smem = smem + OFF_DS + x * DS_TILE;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t off = sw128_offset(row, sub * 4 + ch);
+          *reinterpret_cast<uint4*>(ds_smem + off) =
+              make_uint4(gk[4 * ch], gk[4 * ch + 1], gk[4 * ch + 2], gk[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL));
+      if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL + x));
     }
     // dV (warps 0-3) and dK (warps 4-7) leave TMEM once, after every product.
     if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
@@ -522,41 +522,34 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
     Cursor cur = first;
     for (int it = 0; it < nit; ++it, cur.next(i0, i1)) {
+      const int x = it & 1;
       const int qb = cur.qi * BQ;
       const int bh = cur.hq;
-      if (!ctx.wait(B_DQFULL, it & 1)) break;
+      if (!ctx.wait(B_DQFULL + x, (it >> 1) & 1)) break;
       tc_fence_after();
+      float g[BQ];
+#pragma unroll
+      for (int c = 0; c < BQ / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + 128u * x + 64 + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[c * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE + x));
+      // Per group of 4 queries, transpose within each 4-lane group so that a
+      // lane holds 4 consecutive head-dimension values of one query row:
+      // one warp instruction then adds 4 rows x 128 contiguous bytes.
       const int lim = min(BQ, N - qb);
       float* base = dq_acc + (static_cast<size_t>(bh) * N + qb + (lane & 3)) * HD +
                     quad * 32 + (lane & ~3);
-      // Two halves of 64 queries; R1 is released once the second half has
-      // been read, before its atomics.
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float g[64];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + TM_R1 + 64 * half + c * 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) g[c * 32 + i] = __uint_as_float(r[i]);
-        }
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE));
-        }
-        // Per group of 4 queries, transpose within each 4-lane group so that
-        // a lane holds 4 consecutive head-dimension values of one query row:
-        // one warp instruction then adds 4 rows x 128 contiguous bytes.
-#pragma unroll
-        for (int q0 = 0; q0 < 64; q0 += 4) {
-          float v[4] = {g[q0] * scale, g[q0 + 1] * scale, g[q0 + 2] * scale, g[q0 + 3] * scale};
-          transpose4(v, lane);
-          const int q = 64 * half + q0;
-          if (q + (lane & 3) < lim)
-            red_add_v4(base + static_cast<size_t>(q) * HD, v[0], v[1], v[2], v[3]);
-        }
+      for (int q0 = 0; q0 < BQ; q0 += 4) {
+        float v[4] = {g[q0] * scale, g[q0 + 1] * scale, g[q0 + 2] * scale, g[q0 + 3] * scale};
+        transpose4(v, lane);
+        if (q0 + (lane & 3) < lim)
+          red_add_v4(base + static_cast<size_t>(q0) * HD, v[0], v[1], v[2], v[3]);
       }
     }
   }
