@@ -46,6 +46,7 @@ SIGNATURES = {
     "fa_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "fa_get_device_status": (_I, [_P]),
     "fa_set_timing_events": (_I, [_P, _P]),
+    "fa_selftest_timeout": (_I, [ctypes.c_uint, _P]),
     "fa_last_error": (ctypes.c_char_p, []),
 }
 
@@ -148,6 +149,10 @@ def fa_workspace_size(op, B, H, n_or_lkv, d, num_splits):
 
 def fa_get_device_status(stream):
     return _call("fa_get_device_status", stream)
+
+
+def fa_selftest_timeout(limit_ms, stream):
+    return _call("fa_selftest_timeout", limit_ms, stream)
 
 
 def fa_set_timing_events(before, after):

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -100,6 +101,10 @@ int make_map_u8(CUtensorMap* map, const void* base, int heads, int rows, int inn
 // pool returns them to the system at every synchronisation, which makes each
 // call pay for a fresh mapping).
 cudaError_t workspace_alloc(void** p, size_t bytes, cudaStream_t stream) {
+  // Fault injection for tests: FA_DEBUG_FAIL_ALLOC=1 makes every workspace
+  // allocation fail as if the device were out of memory.
+  const char* inject = std::getenv("FA_DEBUG_FAIL_ALLOC");
+  if (inject != nullptr && inject[0] == '1') return cudaErrorMemoryAllocation;
   static std::mutex mu;
   static cudaMemPool_t pools[fa::kMaxDevices] = {};
   int dev = -1;
@@ -486,7 +491,8 @@ int fa_get_device_status(cudaStream_t stream) {
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
   int s = 0;
   const int parts[] = {fa::status_forward_fp32(true), fa::status_forward_bf16(true),
-                       fa::status_backward_bf16(true), fa::status_decode(true)};
+                       fa::status_backward_bf16(true), fa::status_decode(true),
+                       fa::status_selftest(true)};
   for (int p : parts)
     if (p != 0) s = p;
   e = cudaGetLastError();
@@ -494,6 +500,14 @@ int fa_get_device_status(cudaStream_t stream) {
   if (s == fa::kStatusTimeout) return fail(FA_ERR_TIMEOUT, "a kernel wait ran out of time");
   if (s != 0) return fail(FA_ERR_CUDA, "a kernel failed its launch-layout self-check (code %d)", s);
   return ok();
+}
+
+int fa_selftest_timeout(unsigned limit_ms, cudaStream_t stream) {
+  if (limit_ms < 1 || limit_ms > 10000)
+    return fail(FA_ERR_INVALID_ARG, "fa_selftest_timeout: limit_ms must be in [1, 10000]");
+  return launch_result(fa::launch_selftest_timeout(static_cast<uint64_t>(limit_ms) * 1000000ull,
+                                                   stream),
+                       "fa_selftest_timeout launch");
 }
 
 int fa_set_timing_events(cudaEvent_t before, cudaEvent_t after) {

@@ -61,19 +61,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // the wait gave up: either another role of the CTA already aborted
 // (*abort != 0) or this wait ran past FA_WAIT_LIMIT_NS, in which case the
 // abort flag is raised and the timeout recorded in *status.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort, int* status) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int* abort, int* status,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > FA_WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       atomicExch(status, kStatusTimeout);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort, int* status) {
+  return mbar_wait_limit(bar, parity, abort, status, FA_WAIT_LIMIT_NS);
 }
 
 // ---------------------------------------------------------------- TMA

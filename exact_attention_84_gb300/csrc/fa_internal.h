@@ -85,6 +85,10 @@ constexpr size_t kNoAllocMaxParts = 16384;
 constexpr int kMaxDevices = 64;
 cudaError_t decode_noalloc_scratch(void** out, size_t* bytes);
 
+// ---- the timeout path of the bounded waits (selftest.cu)
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream);
+int status_selftest(bool clear);
+
 // Round a byte count up to 256.
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 

@@ -319,6 +319,21 @@ size_t fa_workspace_size(int op, int B, int H, int n_or_lkv, int d,
 int fa_get_device_status(cudaStream_t stream);
 
 /*
+ * fa_selftest_timeout -- diagnostic for the timeout path.  Launches one
+ * thread block that waits, with the same bounded wait the kernels use but a
+ * limit of limit_ms milliseconds (1 .. 10000), on an mbarrier that nothing
+ * completes.  The wait runs out, records FA_ERR_TIMEOUT in the device status
+ * word and the block exits normally (no trap or fault; the context stays
+ * usable), so the next fa_get_device_status on that stream returns
+ * FA_ERR_TIMEOUT and clears it.  Returns FA_OK once launched.
+ *
+ * Host-side fault injection: with the environment variable
+ * FA_DEBUG_FAIL_ALLOC=1 every workspace allocation of the library fails and
+ * the calls that need one return FA_ERR_NO_MEMORY without launching.
+ */
+int fa_selftest_timeout(unsigned limit_ms, cudaStream_t stream);
+
+/*
  * fa_set_timing_events -- measurement hook.  While set (both non-NULL), every
  * later call made on this host thread records `before` on its stream just
  * before launching its main kernel (the fused forward kernel, the backward

@@ -114,6 +114,12 @@ def test_gqa_window_validation(lib):
     assert d(FAKE, None, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
 
 
+def test_selftest_validation(lib):
+    E = _lib
+    assert E.fa_selftest_timeout(0, None) == E.FA_ERR_INVALID_ARG
+    assert E.fa_selftest_timeout(20000, None) == E.FA_ERR_INVALID_ARG
+
+
 def test_workspace_sizes(lib):
     E = _lib
     assert E.fa_workspace_size(E.FA_OP_FORWARD, 1, 1, 8, 128, 0) == 0
