@@ -392,6 +392,12 @@ def run_ours(args, dist: Dist):
         "gpu_launches": 4 * args.steps,
         "step": step_parts, "roofline": roofline, "e2e": e2e, "targets": targets,
         "cpu_baseline": cpu, "clocks": clk,
+        # O(N) memory: the only device memory beyond inputs and outputs is the
+        # backward workspace (fp32 dQ accumulator + two padded stat rows), no
+        # N x N buffer; per head against the N^2 bf16 score matrix it avoids
+        "memory": {"forward_workspace_bytes": 0, "backward_workspace_bytes": ws_bytes,
+                   "backward_workspace_bytes_per_head": ws_bytes // (B * H),
+                   "n2_bf16_bytes_per_head": N * N * 2},
     }
 
 

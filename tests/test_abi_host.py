@@ -114,6 +114,17 @@ def test_gqa_window_validation(lib):
     assert d(FAKE, None, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
 
 
+def test_size_limits(lib):
+    """Sizes past what the kernels index are refused before any launch."""
+    E = _lib
+    assert E.fa_forward(FAKE, FAKE, FAKE, FAKE, None, 1, 1, (1 << 30) + 1, 128, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert E.fa_forward(FAKE, FAKE, FAKE, FAKE, None, 1 << 16, 1 << 15, 8, 128, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert E.fa_decode(FAKE, FAKE, FAKE, FAKE, 256, 256, 100, 128, 1, None) == E.FA_ERR_UNSUPPORTED
+    assert E.fa_forward_fp32(FAKE, FAKE, FAKE, FAKE, None, 256, 256, 8, 64, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert E.fa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, None, 64, 32, 32768, 128, 16, 0.1, None) == E.FA_ERR_UNSUPPORTED
+    assert "scratch" in E.fa_last_error()
+
+
 def test_selftest_validation(lib):
     E = _lib
     assert E.fa_selftest_timeout(0, None) == E.FA_ERR_INVALID_ARG
