@@ -44,6 +44,7 @@ SIGNATURES = {
     "fa_decode_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _Z, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "fa_decode_splits": (_I, [_I, _I, _I, _I]),
     "fa_get_device_status": (_I, [_P]),
     "fa_set_timing_events": (_I, [_P, _P]),
     "fa_selftest_timeout": (_I, [ctypes.c_uint, _P]),
@@ -141,6 +142,10 @@ def fa_decode_ex(q, kcache, vcache, o, lse_out, B, H, Lkv, d, num_splits, scale,
 def fa_decode_noalloc(q, kcache, vcache, o, lse_out, B, H, Lkv, d, num_splits, scale, stream):
     return _call("fa_decode_noalloc", q, kcache, vcache, o, lse_out, B, H, Lkv, d, num_splits,
                  scale, stream)
+
+
+def fa_decode_splits(B, Hq, Hkv, Lkv):
+    return _call("fa_decode_splits", B, Hq, Hkv, Lkv)
 
 
 def fa_workspace_size(op, B, H, n_or_lkv, d, num_splits):

@@ -125,14 +125,15 @@ def decode(q, kcache, vcache, num_splits: int = 1, scale: float | None = None,
     """o (and optionally lse) for one query token per (b, h): q [B, H, d],
     caches [B, Hkv, Lkv, d], all bf16 (H a multiple of Hkv: query head h
     reads cache head h // (H // Hkv)).  ``alibi_slopes``: H fp32 slopes; the
-    new token is at position Lkv - 1."""
+    new token is at position Lkv - 1.  ``num_splits=0`` lets the library
+    choose (grouped or ALiBi calls)."""
     B, Hkv, L, d = kcache.shape
     H = q.shape[1]
     for t, n in ((q, "q"), (kcache, "kcache"), (vcache, "vcache")):
         _need(t, torch.bfloat16, n)
     o = torch.empty_like(q)
     lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if with_lse else None
-    if Hkv != H or alibi_slopes is not None:
+    if Hkv != H or alibi_slopes is not None or num_splits == 0:
         scale = 1.0 / math.sqrt(d) if scale is None else scale
         ws_ptr = workspace.data_ptr() if workspace is not None else None
         ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
@@ -157,3 +158,33 @@ def decode(q, kcache, vcache, num_splits: int = 1, scale: float | None = None,
 def device_status() -> int:
     """Synchronise the current stream and return the kernels' status word."""
     return _lib.fa_get_device_status(_stream())
+
+
+class _Attention(torch.autograd.Function):
+    """Autograd node over ``forward`` / ``backward`` (bf16): saves Q, K, V,
+    O and LSE, and returns dQ, dK, dV from the recomputation backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, window, alibi_slopes, deterministic):
+        o, lse = forward(q, k, v, causal=causal, scale=scale, window=window,
+                         alibi_slopes=alibi_slopes)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.opts = (causal, scale, window, alibi_slopes, deterministic)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        causal, scale, window, alibi_slopes, deterministic = ctx.opts
+        dq, dk, dv = backward(q, k, v, o, lse, do.contiguous(), causal=causal, scale=scale,
+                              window=window, alibi_slopes=alibi_slopes,
+                              deterministic=deterministic)
+        return dq, dk, dv, None, None, None, None, None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0,
+              alibi_slopes=None, deterministic: bool = False):
+    """Differentiable attention for bf16 [B, H, N, d] q and [B, Hkv, N, d]
+    k, v: O = softmax(scale Q K^T [+ mask, ALiBi]) V, with dQ, dK, dV from
+    the library's backward when autograd asks for them."""
+    return _Attention.apply(q, k, v, causal, scale, window, alibi_slopes, deterministic)

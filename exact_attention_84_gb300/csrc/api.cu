@@ -384,6 +384,30 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
   return launch_result(e, "fa_decode launch");
 }
 
+int fa_decode_splits(int B, int Hq, int Hkv, int Lkv) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lkv < 1 || Hq % Hkv != 0) return 0;
+  // Thread blocks per split: one per (b, h) for one query head per cache
+  // head, one per (b, cache head, 16 query heads) otherwise; two fit an SM.
+  // Aim at about 16 waves of blocks so the last wave is a small part of the
+  // work, with at least 512 cache rows per split.
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    cudaGetLastError();
+    sms = 148;
+  }
+  const int g = Hq / Hkv;
+  const long long units = g == 1 ? static_cast<long long>(B) * Hq
+                                 : static_cast<long long>(B) * Hkv * ((g + 15) / 16);
+  const long long want = (16ll * 2 * sms + units - 1) / units;
+  long long s = want < 1 ? 1 : want;
+  const long long by_len = Lkv / 512 > 1 ? Lkv / 512 : 1;
+  if (s > by_len) s = by_len;
+  if (s > 1024) s = 1024;
+  if (s > Lkv) s = Lkv;
+  return static_cast<int>(s);
+}
+
 int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o,
                   float* lse_out, int B, int Hq, int Hkv, int Lkv, int d, int num_splits,
                   float scale, const float* alibi_slopes, void* ws, size_t ws_bytes,
@@ -394,8 +418,10 @@ int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o
   if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
   if (int r = check_scale(scale)) return r;
   if (int r = check_heads(fn, Hq, Hkv, 0, 0)) return r;
+  if (num_splits == 0) num_splits = fa_decode_splits(B, Hq, Hkv, Lkv);
   if (num_splits < 1 || num_splits > Lkv || num_splits > 1024)
-    return fail(FA_ERR_INVALID_ARG, "%s: num_splits must be in [1, min(Lkv, 1024)] (got %d)", fn,
+    return fail(FA_ERR_INVALID_ARG,
+                "%s: num_splits must be 0 (automatic) or in [1, min(Lkv, 1024)] (got %d)", fn,
                 num_splits);
   const int group = Hq / Hkv;
   if (static_cast<long long>(B) * Hkv * ((group + 15) / 16) > 65535ll ||

@@ -265,12 +265,22 @@ int fa_decode_ex(const void* q, const void* kcache, const void* vcache, void* o,
  *             fa_forward_gqa).
  *   Hkv >= 1, Hq % Hkv == 0, B*Hq <= 65535.  Splits, scale and workspace as
  *   in fa_decode_ex, with the workspace sized by
- *   fa_workspace_size(FA_OP_DECODE, B, Hq, Lkv, d, num_splits).
+ *   fa_workspace_size(FA_OP_DECODE, B, Hq, Lkv, d, num_splits); num_splits
+ *   0 takes fa_decode_splits(B, Hq, Hkv, Lkv) (size a caller workspace with
+ *   that value).
  */
 int fa_decode_gqa(const void* q, const void* kcache, const void* vcache, void* o,
                   float* lse_out, int B, int Hq, int Hkv, int Lkv, int d,
                   int num_splits, float scale, const float* alibi_slopes, void* ws,
                   size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * fa_decode_splits -- the split count fa_decode_gqa uses for num_splits = 0:
+ * enough thread blocks for about 16 waves on the current device, at least
+ * 512 cache rows per split, at most min(Lkv, 1024).  Returns 0 for invalid
+ * sizes.
+ */
+int fa_decode_splits(int B, int Hq, int Hkv, int Lkv);
 
 /*
  * fa_decode_noalloc -- fa_decode_ex without any allocation.  The pages have

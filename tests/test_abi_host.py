@@ -109,7 +109,7 @@ def test_gqa_window_validation(lib):
               None) == E.FA_ERR_INVALID_ARG
     d = E.fa_decode_gqa
     assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 3, 100, 128, 2, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
-    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 0, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
+    assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, -1, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
     assert d(FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, FAKE, 8, None) == E.FA_ERR_INVALID_ARG
     assert d(FAKE, None, FAKE, FAKE, None, 1, 8, 2, 100, 128, 2, 0.1, None, None, 0, None) == E.FA_ERR_INVALID_ARG
 
@@ -123,6 +123,14 @@ def test_size_limits(lib):
     assert E.fa_forward_fp32(FAKE, FAKE, FAKE, FAKE, None, 256, 256, 8, 64, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
     assert E.fa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, None, 64, 32, 32768, 128, 16, 0.1, None) == E.FA_ERR_UNSUPPORTED
     assert "scratch" in E.fa_last_error()
+
+
+def test_decode_splits_choice(lib):
+    E = _lib
+    assert E.fa_decode_splits(0, 8, 2, 100) == 0 and E.fa_decode_splits(1, 8, 3, 100) == 0
+    for B, Hq, Hkv, L in ((64, 32, 32, 32768), (64, 32, 8, 32768), (1, 1, 1, 10), (1, 64, 1, 300000)):
+        s = E.fa_decode_splits(B, Hq, Hkv, L)
+        assert 1 <= s <= min(L, 1024) and (s == 1 or L // s >= 512)
 
 
 def test_selftest_validation(lib):

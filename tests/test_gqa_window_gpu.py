@@ -157,3 +157,12 @@ def test_gqa_decode_b64_hq32_hkv8_l32768_sampled():
     base = outs[1][0].float()
     for s in (2, 4, 8):
         assert (outs[s][0].float() - base).abs().max().item() <= O_MAX
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L", [(2, 8, 2, 5000), (4, 4, 4, 3000)])
+def test_decode_automatic_splits(B, Hq, Hkv, L):
+    q, kc, vc = inputs.decode_gqa_inputs(B, Hq, Hkv, L, D, torch.bfloat16, 140 + L, "cuda")
+    assert _lib.fa_decode_splits(B, Hq, Hkv, L) >= 1
+    o, lse = api.decode(q, kc, vc, num_splits=0, scale=SCALE, with_lse=True)
+    o_ref, lse_ref = orc.attention_decode_gqa(np64(q), np64(kc), np64(vc), SCALE)
+    assert_close_bf16(o, lse, o_ref, lse_ref, f"L={L} automatic splits")
