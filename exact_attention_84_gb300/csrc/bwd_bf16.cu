@@ -851,17 +851,17 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   (void)q;
   (void)k;
   (void)v;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
     cudaError_t e = set_smem(bwd_main_kernel<false, true>);
     if (e == cudaSuccess) e = set_smem(bwd_main_kernel<true, true>);
     if (e == cudaSuccess) e = set_smem(bwd_main_kernel<false, false>);
     if (e == cudaSuccess) e = set_smem(bwd_main_kernel<true, false>);
     if (e == cudaSuccess) e = set_smem(bwd_dq_kernel<false>, DQ_SMEM);
     if (e == cudaSuccess) e = set_smem(bwd_dq_kernel<true>, DQ_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   const int BH = B * H;
   const int Npad = static_cast<int>(padded_len(N));
   const size_t rows = static_cast<size_t>(BH) * N;

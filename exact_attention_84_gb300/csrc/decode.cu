@@ -508,14 +508,12 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
                           float* lse_out, int B, int H, int L, int num_splits, float scale,
                           void* ws, cudaStream_t stream, const TimingEvents& ev,
                           const float* alibi) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SMEM_BYTES));
+  });
+  if (ea != cudaSuccess) return ea;
   const int BH = B * H;
   const size_t parts = static_cast<size_t>(BH) * num_splits;
   float* part_o = static_cast<float*>(ws);
@@ -539,14 +537,13 @@ cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, co
                               void* o, float* lse_out, int B, int Hq, int Hkv, int L,
                               int num_splits, float scale, void* ws, cudaStream_t stream,
                               const TimingEvents& ev, const float* alibi) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gqa_split_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(G_SMEM));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(decode_gqa_split_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(G_SMEM));
+  });
+  if (ea != cudaSuccess) return ea;
   const int group = Hq / Hkv;
   const int nslice = (group + 15) / 16;
   const size_t parts = static_cast<size_t>(B) * Hq * num_splits;

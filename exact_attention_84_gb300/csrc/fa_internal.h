@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -88,6 +89,23 @@ cudaError_t decode_noalloc_scratch(void** out, size_t* bytes);
 // ---- the timeout path of the bounded waits (selftest.cu)
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream);
 int status_selftest(bool clear);
+
+// Runs `setup` (e.g. the cudaFuncSetAttribute calls of a launcher) once per
+// device: function attributes belong to the device they were set on, so a
+// process that drives several GPUs needs them on each.  `done` holds one bit
+// per device; concurrent first calls may both run `setup`, which is harmless.
+template <class Setup>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, Setup setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t{1} << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = setup();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Round a byte count up to 256.
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }

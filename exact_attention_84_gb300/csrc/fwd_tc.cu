@@ -626,15 +626,15 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
                                 int Hkv, int N, float scale, int causal, int window,
                                 const float* alibi, cudaStream_t stream,
                                 const TimingEvents& ev) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
     cudaError_t e = set_smem(fwd_bf16_kernel<false, false>, Bf16::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<true, false>, Bf16::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<false, true>, Bf16::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(fwd_bf16_kernel<true, true>, Bf16::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   const int BH = B * H;
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -668,15 +668,15 @@ cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, 
                                int N, float scale, float q_descale, float k_descale,
                                float v_descale, int causal, int window, const float* alibi,
                                cudaStream_t stream, const TimingEvents& ev) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t ea = once_per_device(attr_done, [] {
     cudaError_t e = set_smem(fwd_fp8_kernel<false, false>, Fp8::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<true, false>, Fp8::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<false, true>, Fp8::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(fwd_fp8_kernel<true, true>, Fp8::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   const int BH = B * H;
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const float scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
