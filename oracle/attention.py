@@ -127,7 +127,7 @@ def attention_forward_rows(q_rows, k, v, rows, scale: float, causal: bool, windo
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale: float, causal: bool):
+def attention_backward(q, k, v, do, scale: float, causal: bool, o=None):
     """Analytic gradients (dQ, dK, dV) of O = softmax(Q.K^T*scale).V.
 
     P is recomputed from Q and K ("03. FlashAttention", "Backward pass":
@@ -138,8 +138,12 @@ def attention_backward(q, k, v, do, scale: float, causal: bool):
       D_i = sum_j P_ij dP_ij = sum_k dO_ik O_ik
       dS = P * (dP - D)          (softmax Jacobian applied row by row)
       dQ = scale * dS K,  dK = scale * dS^T Q
+    ``o`` (optional): the forward output as stored (e.g. rounded to bf16);
+    the backward keeps O from the forward pass, so D is formed from it.  By
+    default the exact O of the definition is used.
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    o_stored = None if o is None else _f64(o)
     lead = q.shape[:-2]
     n = q.shape[-2]
     rows = np.arange(n)
@@ -148,6 +152,8 @@ def attention_backward(q, k, v, do, scale: float, causal: bool):
     dv = np.empty_like(v)
     for idx in np.ndindex(*lead):
         o, _, p = _head_forward(q[idx], k[idx], v[idx], scale, causal, rows)
+        if o_stored is not None:
+            o = o_stored[idx]
         g = do[idx]
         dv[idx] = p.T @ g
         dp = g @ v[idx].T
@@ -258,10 +264,12 @@ def attention_forward_gqa(q, k, v, scale: float, causal: bool, window=None, alib
 
 
 def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None,
-                           alibi_slopes=None):
+                           alibi_slopes=None, o=None):
     """Gradients for grouped heads: dQ per query head; dK, dV of a key/value
-    head are the sums over the query heads that read it."""
+    head are the sums over the query heads that read it.  ``o``: the stored
+    forward output, as in ``attention_backward``."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    o_given = None if o is None else _f64(o)
     B, hq, n, _ = q.shape
     hkv = k.shape[1]
     rows = np.arange(n)
@@ -273,6 +281,8 @@ def attention_backward_gqa(q, k, v, do, scale: float, causal: bool, window=None,
             g = _kv_head(h, hq, hkv)
             o, _, p = _head_forward(q[b, h], k[b, g], v[b, g], scale, causal, rows, window,
                                     _slope(alibi_slopes, h))
+            if o_given is not None:
+                o = o_given[b, h]
             gr = do[b, h]
             dv[b, g] += p.T @ gr                  # dV summed over the group
             dpg = gr @ v[b, g].T

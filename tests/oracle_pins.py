@@ -262,6 +262,36 @@ def pin_backward_identities(orc):
         assert np.abs(dk.sum(axis=-2)).max() < 1e-12
 
 
+def pin_backward_stored_o(orc):
+    """The backward forms D from the O it is given: with the exact O nothing
+    changes; shifting row i of O by c changes D_i by c * sum_k dO_ik, which
+    moves dQ_i by -scale * dD_i * (P K)_i and dK_j by -scale * sum_i P_ij
+    dD_i Q_i and leaves dV alone."""
+    r = _rng(71)
+    n, d = 6, 4
+    q, k, v, do = (r.standard_normal((1, n, d)) for _ in range(4))
+    o, lse = orc.attention_forward(q, k, v, 0.5, True)
+    base = orc.attention_backward(q, k, v, do, 0.5, True)
+    same = orc.attention_backward(q, k, v, do, 0.5, True, o=o)
+    for a, b in zip(base, same):
+        assert np.abs(a - b).max() < 1e-15
+    shift = np.zeros((1, n, 1))
+    shift[0, 2, 0], shift[0, 4, 0] = 0.3, -0.7
+    moved = orc.attention_backward(q, k, v, do, 0.5, True, o=o + shift)
+    dd = shift[0, :, 0] * do[0].sum(axis=1)                       # change of D_i
+    s = 0.5 * q[0] @ k[0].T
+    s = np.where(np.arange(n)[None, :] > np.arange(n)[:, None], -np.inf, s)
+    p = np.exp(s - lse[0][:, None])
+    want_dq = base[0][0] - 0.5 * dd[:, None] * (p @ k[0])
+    want_dk = base[1][0] - 0.5 * (p * dd[:, None]).T @ q[0]
+    assert np.abs(moved[0][0] - want_dq).max() < 1e-13
+    assert np.abs(moved[1][0] - want_dk).max() < 1e-13
+    assert np.abs(moved[2] - base[2]).max() < 1e-15
+    g = orc.attention_backward_gqa(q[None], k[None], v[None], do[None], 0.5, True, o=(o + shift)[None])
+    for a, b in zip(g, moved):
+        assert np.abs(a[0] - b).max() < 1e-14
+
+
 def pin_torch_sdpa(orc):
     """Library special case: PyTorch's fp64 CPU attention and autograd."""
     import torch
@@ -510,6 +540,7 @@ ALL_PINS = [
     pin_invariances,
     pin_backward_finite_diff,
     pin_backward_identities,
+    pin_backward_stored_o,
     pin_torch_sdpa,
     pin_rows_subset,
     pin_gqa_repeat_kv,

@@ -94,9 +94,12 @@ def test_peaked_softmax(causal):
     o_ref, lse_ref = orc.attention_forward(np64(q), np64(k), np64(v), SCALE, causal)
     assert_close_bf16(o, lse, o_ref, lse_ref, f"causal={causal}")
     grads = api.backward(q, k, v, o, lse, do, causal=causal, scale=SCALE)
-    refs = orc.attention_backward(np64(q), np64(k), np64(v), np64(do), SCALE, causal)
-    for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
-        # dQ and dK scale with |K| and |Q| (x8 here): compare relative to the
-        # gradient's own magnitude, at the 5e-2 tolerance of unit-scale inputs
-        err = np.abs(np64(got) - ref).max() / max(1.0, np.abs(ref).max() / 8.0)
-        assert err <= G_MAX, f"{name} scaled max err {err:.3e}"
+    # The backward forms D = rowsum(dO * O) from the O the forward stored (in
+    # bf16); with a nearly one-hot softmax dP - D cancels, so the reference
+    # takes the same stored O.  dQ and dK scale linearly with |K| and |Q|
+    # (x8 here), so their tolerance is 8 times the unit-scale 5e-2.
+    refs = orc.attention_backward(np64(q), np64(k), np64(v), np64(do), SCALE, causal,
+                                  o=np64(o))
+    for name, got, ref, tol in zip(("dq", "dk", "dv"), grads, refs, (8 * G_MAX, 8 * G_MAX, G_MAX)):
+        err = np.abs(np64(got) - ref).max()
+        assert err <= tol, f"{name} max err {err:.3e} (tolerance {tol:.2e})"
