@@ -453,10 +453,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
           l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
         }
-        float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, l4.x));
-        float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, l4.y));
-        float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), scale_log2, l4.z));
-        float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), scale_log2, l4.w));
+        // exponent arguments and dS = P (dP - D) on packed fp32 pairs
+        const uint64_t sc2 = f2pack(scale_log2, scale_log2);
+        float a0, a1, a2, a3;
+        f2unpack(f2fma(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2,
+                       f2pack(l4.x, l4.y)), a0, a1);
+        f2unpack(f2fma(f2pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sc2,
+                       f2pack(l4.z, l4.w)), a2, a3);
+        float p0 = fast_exp2(a0), p1 = fast_exp2(a1), p2 = fast_exp2(a2), p3 = fast_exp2(a3);
         if (need_mask) {
           // qlo <= q <= qhi as one unsigned compare per query (the
           // wrap-around of rel + t is the exact difference mod 2^32)
@@ -468,10 +472,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         pk[e / 2] = pack_bf16x2(p0, p1);
         pk[e / 2 + 1] = pack_bf16x2(p2, p3);
-        gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + d4.x),
-                                p1 * (__uint_as_float(dr[e + 1]) + d4.y));
-        gk[e / 2 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[e + 2]) + d4.z),
-                                    p3 * (__uint_as_float(dr[e + 3]) + d4.w));
+        {
+          float g0, g1, g2, g3;
+          f2unpack(f2mul(f2pack(p0, p1), f2add(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                               f2pack(d4.x, d4.y))), g0, g1);
+          f2unpack(f2mul(f2pack(p2, p3), f2add(f2pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                               f2pack(d4.z, d4.w))), g2, g3);
+          gk[e / 2] = pack_bf16x2(g0, g1);
+          gk[e / 2 + 1] = pack_bf16x2(g2, g3);
+        }
       }
       // Packed P^T and dS^T go over exactly the 32 columns this thread has
       // just read (P^T first 16, dS^T last 16): no other warp reads them.
