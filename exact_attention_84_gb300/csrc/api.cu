@@ -161,6 +161,14 @@ int check_heads(const char* fn, int Hq, int Hkv, int causal, int window) {
   return FA_OK;
 }
 
+// Grid sizes are computed in int: refuse shapes whose thread-block count
+// (or element count for the elementwise kernels) would not fit.
+int check_grid(const char* fn, long long blocks) {
+  if (blocks > 2147483647ll)
+    return fail(FA_ERR_UNSUPPORTED, "%s: the problem needs more than 2^31-1 thread blocks", fn);
+  return FA_OK;
+}
+
 int launch_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess)
     return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -179,6 +187,7 @@ static int forward_impl(const char* fn, const void* q, const void* k, const void
   if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
   if (int r = check_scale(scale)) return r;
   if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
+  if (int r = check_grid(fn, (N + 255ll) / 256 * B * Hq)) return r;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
       (alibi && (reinterpret_cast<uintptr_t>(alibi) & 3u)))
@@ -219,6 +228,7 @@ int fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* 
     if (!std::isfinite(x) || !(x > 0.f))
       return fail(FA_ERR_INVALID_ARG, "%s: descale factors must be finite and > 0", fn);
   if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
+  if (int r = check_grid(fn, (N + 255ll) / 256 * B * Hq)) return r;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
       (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)))
@@ -285,6 +295,13 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
   if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
   if (int r = check_scale(scale)) return r;
   if (int r = check_heads(fn, Hq, Hkv, causal, window)) return r;
+  {
+    const long long padded = (N + 127ll) / 128 * 128 * B * Hq;        // bwd_pre rows
+    if (int r = check_grid(fn, (N + 127ll) / 128 * B * Hkv)) return r;
+    if (int r = check_grid(fn, (padded + 15) / 16)) return r;
+    if (int r = check_grid(fn, static_cast<long long>(B) * Hq * N / 16 + 1)) return r;  // convert
+    if (int r = check_grid(fn, (N + 127ll) / 128 * B * Hq)) return r;   // deterministic dQ
+  }
   const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);

@@ -121,6 +121,11 @@ def test_size_limits(lib):
     assert E.fa_forward(FAKE, FAKE, FAKE, FAKE, None, 1 << 16, 1 << 15, 8, 128, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
     assert E.fa_decode(FAKE, FAKE, FAKE, FAKE, 256, 256, 100, 128, 1, None) == E.FA_ERR_UNSUPPORTED
     assert E.fa_forward_fp32(FAKE, FAKE, FAKE, FAKE, None, 256, 256, 8, 64, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
+    # per-dimension limits pass, the thread-block count does not
+    assert E.fa_forward(FAKE, FAKE, FAKE, FAKE, None, 1 << 10, 1 << 10, 1 << 20, 128, 0.1, 0, None) == E.FA_ERR_UNSUPPORTED
+    assert "2^31" in E.fa_last_error()
+    args9 = [FAKE] * 9
+    assert E.fa_backward(*args9, 1 << 10, 1 << 10, 1 << 20, 128, 0.1, 1, None) == E.FA_ERR_UNSUPPORTED
     assert E.fa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, None, 64, 32, 32768, 128, 16, 0.1, None) == E.FA_ERR_UNSUPPORTED
     assert "scratch" in E.fa_last_error()
 
