@@ -196,6 +196,7 @@ static int forward_impl(const char* fn, const void* q, const void* k, const void
   if (int r = make_map(&maps.q, q, B * Hq, N, 128)) return r;
   if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
+  if (int r = make_map(&maps.o, o, B * Hq, N, 128)) return r;
   return launch_result(fa::launch_forward_bf16(maps, o, lse, B, Hq, Hkv, N, scale, causal,
                                                window >= N ? 0 : window, alibi, stream,
                                                g_events),
@@ -320,6 +321,8 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
   if (int r = make_map(&maps.dO, dO, B * Hq, N, 64)) return r;
   if (int r = make_map(&maps.k, k, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
+  if (int r = make_map(&maps.dk, dk, B * Hkv, N, 128)) return r;
+  if (int r = make_map(&maps.dv, dv, B * Hkv, N, 128)) return r;
   if (deterministic) {                                            // 128-query blocks, 64-key tiles
     if (int r = make_map(&dq_maps.q, q, B * Hq, N, 128)) return r;
     if (int r = make_map(&dq_maps.dO, dO, B * Hq, N, 128)) return r;

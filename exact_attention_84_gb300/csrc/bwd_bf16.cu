@@ -80,7 +80,8 @@ constexpr int B_PFULL = B_SFULL + 2;       // + buffer: P^T, dS^T written (8 war
 constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
 constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
 constexpr int B_DONE = B_DQFREE + 2;       // every product of the block completed
-constexpr int NBAR = B_DONE + 1;
+constexpr int B_EPI = B_DONE + 1;          // + (0 dV, 1 dK): staged in shared memory (4 warps)
+constexpr int NBAR = B_EPI + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // base is 1024-aligned (checked)
 
@@ -196,9 +197,9 @@ template <bool kAlibi, bool kDq>
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                 const float* __restrict__ lse_pad, const float* __restrict__ d_pad,
-                float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dK,
-                __nv_bfloat16* __restrict__ dV, int BHkv, int N, int Npad, float scale,
+                float* __restrict__ dq_acc, int BHkv, int N, int Npad, float scale,
                 int causal, int qgroup, int window, int head_group,
                 const float* __restrict__ alibi, int heads) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -257,6 +258,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_DQFREE + x), 4);
     }
     mbar_init(bar_addr(sbase, B_DONE), 1);
+    mbar_init(bar_addr(sbase, B_EPI + 0), 4);
+    mbar_init(bar_addr(sbase, B_EPI + 1), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -276,6 +279,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
+      prefetch_tmap(&tmdK);
+      prefetch_tmap(&tmdV);
       const uint32_t kvf = bar_addr(sbase, B_KVFULL);
       mbar_arrive_expect_tx(kvf, 2 * TILE);
       tma_load_3d(sbase + OFF_K, &tmK, kvf, 0, j * BKV, bkv);
@@ -502,27 +507,38 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(sbase, B_PFULL + x));
     }
-    // dV (warps 0-3) and dK (warps 4-7) leave TMEM once, after every product.
+    // dV (warps 0-3) and dK (warps 4-7) leave TMEM once, after every
+    // product.  K_j and V_j are no longer read then, so each gradient is
+    // staged over the tile it belongs to (dV over V_j, dK over K_j) in the
+    // same swizzled boxes and leaves with one bulk tensor store, which also
+    // drops the rows past N.
     if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
       tc_fence_after();
-      __nv_bfloat16* out = sub == 0 ? dV : dK;
       const float mul = sub == 0 ? 1.f : scale;
       const uint32_t src = tmem + lane_addr + (sub == 0 ? TM_DV : TM_DK);
+      const uint32_t stage = sub == 0 ? OFF_V : OFF_K;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(src + c * 32, r);
-        if (kv < N) {
-          uint4* d4 =
-              reinterpret_cast<uint4*>(out + (static_cast<size_t>(bkv) * N + kv) * HD + c * 32);
+        uint8_t* box = smem + stage + (c >> 1) * HALF;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * i]) * mul, __uint_as_float(r[8 * i + 1]) * mul),
-                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul),
-                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul),
-                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
-        }
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(box + sw128_offset(row, (c & 1) * 4 + i)) = make_uint4(
+              pack_bf16x2(__uint_as_float(r[8 * i]) * mul, __uint_as_float(r[8 * i + 1]) * mul),
+              pack_bf16x2(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul),
+              pack_bf16x2(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul),
+              pack_bf16x2(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(sbase, B_EPI + sub));
+      if (quad == 0 && lane == 0 && ctx.wait(B_EPI + sub, 0)) {
+        const CUtensorMap* map = sub == 0 ? &tmdV : &tmdK;
+        tma_store_3d(map, sbase + stage, 0, j * BKV, bkv);
+        tma_store_3d(map, sbase + stage + HALF, 64, j * BKV, bkv);
+        bulk_commit_group();
+        bulk_wait_group_read0();   // the block may exit once the tiles have been read
       }
     }
   } else if (kDq) {
@@ -857,7 +873,9 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
                                  int Hkv, int N, float scale, int causal, int window,
                                  const float* alibi, const BwdMaps* dq_maps, void* ws,
                                  cudaStream_t stream, const TimingEvents& ev) {
-  (void)q;
+  (void)q;   // the tensors behind the maps
+  (void)dk;
+  (void)dv;
   (void)k;
   (void)v;
   static std::atomic<uint64_t> attr_done{0};
@@ -894,9 +912,8 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
                     ? (alibi ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>)
                     : (alibi ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>);
   kernel<<<dim3(nkv * B * Hkv), dim3(NTHREADS), SMEM_BYTES, stream>>>(
-      maps.q, maps.k, maps.v, maps.dO, lse_pad, d_pad, dq_acc, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), B * Hkv, N, Npad, scale, causal, g, window, head_group,
-      alibi, H);
+      maps.q, maps.k, maps.v, maps.dO, maps.dk, maps.dv, lse_pad, d_pad, dq_acc, B * Hkv, N,
+      Npad, scale, causal, g, window, head_group, alibi, H);
   e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;

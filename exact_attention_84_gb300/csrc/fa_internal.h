@@ -24,9 +24,9 @@ cudaError_t launch_forward_fp32(const float* q, const float* k, const float* v, 
 int status_forward_fp32(bool clear);
 
 // ---- bf16 tcgen05 forward (fwd_tc.cu); tensor maps over [B*H, N, 128]
-// (Q) and [B*Hkv, N, 128] (K, V); window 0 = none.
+// (Q and the bf16 output O) and [B*Hkv, N, 128] (K, V); window 0 = none.
 struct FwdMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, o;
 };
 // alibi: device array of H slopes (ALiBi bias -slope_h |i - j|) or nullptr.
 cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
@@ -50,11 +50,11 @@ cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, 
 
 // ---- bf16 backward (bwd_bf16.cu)
 struct BwdMaps {
-  CUtensorMap q, k, v, dO;
+  CUtensorMap q, k, v, dO, dk, dv;
 };
 size_t backward_workspace_bytes(int B, int H, int N);
 // Q, dO, O, LSE, dQ have H query heads; K, V, dK, dV have Hkv (H % Hkv == 0).
-// maps: Q, dO with 64-row boxes, K, V with 128-row boxes.  dq_maps: nullptr,
+// maps: Q, dO with 64-row boxes, K, V, dK, dV with 128-row boxes.  dq_maps: nullptr,
 // or (deterministic dQ) Q, dO with 128-row boxes and K, V with 64-row boxes.
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,

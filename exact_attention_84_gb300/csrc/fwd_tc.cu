@@ -88,7 +88,8 @@ struct FwdLayout {
   static constexpr int B_SFULL = B_EMPTY + SLOTS;   // + block (A = 0, B = 1)
   static constexpr int B_PFULL = B_SFULL + 2;       // + block
   static constexpr int B_ODONE = B_PFULL + 2;       // + block
-  static constexpr int NBAR = B_ODONE + 2;
+  static constexpr int B_OSTG = B_ODONE + 2;        // + block: O staged (4 warps arrive)
+  static constexpr int NBAR = B_OSTG + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
 };
@@ -114,6 +115,9 @@ struct Bf16 : FwdLayout<BM * HD * 2, 4> {
   static constexpr uint32_t IDESC_O = idesc_bf16(BM, HD, false, true);
   static constexpr int P_COLS = BN / 2;             // packed P: 2 keys per TMEM column
   static constexpr bool kSplitChains = false;       // row max as one chain
+  // O leaves through the block's Q tile (same two swizzled boxes) and one
+  // bulk tensor store, instead of per-row stores from every thread.
+  static constexpr bool kStoreTma = true;
 
   // a 128-row tile of Q or K (rows `row`.., head `head`)
   __device__ static void load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int row,
@@ -167,6 +171,7 @@ struct Fp8 : FwdLayout<BM * HD, 8> {
   static constexpr uint32_t IDESC_O = idesc_e4m3(BM, HD);
   static constexpr int P_COLS = BN / 4;             // packed P: 4 keys per TMEM column
   static constexpr bool kSplitChains = true;        // row max as 8 parallel chains
+  static constexpr bool kStoreTma = false;          // a Q tile (16 KB) cannot hold bf16 O
 
   __device__ static void load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int row,
                                    int head) {
@@ -226,7 +231,8 @@ struct Ctx {
 // multiplies O at the end (the fp8 V descale; 1 for bf16).
 template <class T, bool kWindow, bool kAlibi>
 __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                         const CUtensorMap* tmV, __nv_bfloat16* __restrict__ O,
+                                         const CUtensorMap* tmV, const CUtensorMap* tmO,
+                                         __nv_bfloat16* __restrict__ O,
                                          float* __restrict__ LSE, int BH, int N,
                                          float scale_log2, float out_scale, int causal,
                                          int group, int window, const float* __restrict__ alibi,
@@ -265,6 +271,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       mbar_init(ctx.bar(T::B_SFULL + b), 1);
       mbar_init(ctx.bar(T::B_PFULL + b), 4);
       mbar_init(ctx.bar(T::B_ODONE + b), 1);
+      mbar_init(ctx.bar(T::B_OSTG + b), 4);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -284,6 +291,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       prefetch_tmap(tmQ);
       prefetch_tmap(tmK);
       prefetch_tmap(tmV);
+      if constexpr (T::kStoreTma) prefetch_tmap(tmO);
       const uint32_t qf = ctx.bar(T::B_QFULL);
       const int q0 = pair * 2 * BM;
       mbar_arrive_expect_tx(qf, 2 * T::TILE);
@@ -523,20 +531,49 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     if (ok && ctx.wait(T::B_ODONE + blk, 0)) {
       tc_fence_after();
       const float inv_l = out_scale / l;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * HD;
+      auto pack8 = [&](const uint32_t (&r)[32], int i) {
+        return make_uint4(
+            pack_bf16x2(__uint_as_float(r[8 * i]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+            pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+            pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+            pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+      };
+      if constexpr (T::kStoreTma) {
+        // Every product of this block has completed, so its Q tile is free:
+        // the row goes there in the tile's own swizzled layout (columns
+        // 32c.. of the row = 16-byte chunks 4(c&1).. of box c>>1), and one
+        // thread stores both boxes with the bulk tensor engine, which also
+        // drops the rows past N.
+        const uint32_t stage = blk ? T::OFF_QB : T::OFF_QA;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_addr + c * 32, r);
-        if (q_row < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+          uint8_t* box = smem + stage + (c >> 1) * T::HALF;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * i]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
-                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
-                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
-                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+            *reinterpret_cast<uint4*>(box + sw128_offset(row, (c & 1) * 4 + i)) = pack8(r, i);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ctx.bar(T::B_OSTG + blk));
+        if (quad == 0 && lane == 0 && ctx.wait(T::B_OSTG + blk, 0)) {
+          tma_store_3d(tmO, sbase + stage, 0, qt * BM, bh);
+          tma_store_3d(tmO, sbase + stage + T::HALF, 64, qt * BM, bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // the block may exit once the tile has been read
+        }
+      } else {
+        __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+          if (q_row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pack8(r, i);
+          }
         }
       }
       if (LSE != nullptr && q_row < N)
@@ -556,11 +593,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
 template <bool kWindow, bool kAlibi>
 __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                float* __restrict__ LSE, int BH, int N, float scale_log2, int causal,
-                int group, int window, const float* __restrict__ alibi, int heads) {
-  fwd_body<Bf16, kWindow, kAlibi>(&tmQ, &tmK, &tmV, O, LSE, BH, N, scale_log2, 1.f, causal,
-                                  group, window, alibi, heads);
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int BH, int N,
+                float scale_log2, int causal, int group, int window,
+                const float* __restrict__ alibi, int heads) {
+  fwd_body<Bf16, kWindow, kAlibi>(&tmQ, &tmK, &tmV, &tmO, O, LSE, BH, N, scale_log2, 1.f,
+                                  causal, group, window, alibi, heads);
 }
 
 // Q, K e4m3 [BH, N, 128]; tmV maps the transposed copy V^T [BH, 128, keys].
@@ -570,8 +608,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmVt, __nv_bfloat16* __restrict__ O,
                float* __restrict__ LSE, int BH, int N, float scale_log2, float v_descale,
                int causal, int group, int window, const float* __restrict__ alibi, int heads) {
-  fwd_body<Fp8, kWindow, kAlibi>(&tmQ, &tmK, &tmVt, O, LSE, BH, N, scale_log2, v_descale,
-                                 causal, group, window, alibi, heads);
+  fwd_body<Fp8, kWindow, kAlibi>(&tmQ, &tmK, &tmVt, nullptr, O, LSE, BH, N, scale_log2,
+                                 v_descale, causal, group, window, alibi, heads);
 }
 
 // V [rows, 128] e4m3 -> V^T [128, ld] per head, 64 keys x 128 columns per
@@ -653,8 +691,8 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
                                     : fwd_bf16_kernel<false, false>);
   if (ev.before) cudaEventRecord(ev.before, stream);
   kernel<<<dim3(npair * BH), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
-      maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, causal,
-      H / Hkv, window, alibi, H);
+      maps.q, maps.k, maps.v, maps.o, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2,
+      causal, H / Hkv, window, alibi, H);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;
