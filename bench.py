@@ -98,6 +98,12 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def weak_scaling_value(flops_per_rank_step: float, world: int, ms_step_max: float) -> float:
+    """Whole-job TFLOP/s: every rank runs the same replica, so the work of all
+    ranks in one step over the slowest rank's step time."""
+    return flops_per_rank_step * world / (ms_step_max * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
@@ -279,7 +285,7 @@ def run_ours(args, dist: Dist):
     ms_step = total_ms / args.steps
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    value = (fwd_fl + bwd_fl) * dist.world / (ms_step * 1e-3) / 1e12
+    value = weak_scaling_value(fwd_fl + bwd_fl, dist.world, ms_step)
 
     # --- end to end through the public API with host buffers.  Every step
     # copies its four inputs in from pinned host memory and its three
