@@ -236,7 +236,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
                                          float* __restrict__ LSE, int BH, int N,
                                          float scale_log2, float out_scale, int causal,
                                          int group, int window, const float* __restrict__ alibi,
-                                         int heads) {
+                                         int heads, int nsplit) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -251,9 +251,18 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
 
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const int nkv = (N + BN - 1) / BN;
-  const int pair = causal ? (npair - 1 - static_cast<int>(blockIdx.x) / BH)
-                          : (static_cast<int>(blockIdx.x) / BH);
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // Work items are (Q pair, head); the last nsplit items (non-causal only)
+  // are split into two thread blocks of one Q tile each, so that a last
+  // wave of items that would keep few SMs busy for a whole item runs as
+  // twice as many half-length blocks.
+  const int nfull = npair * BH - nsplit;
+  const int bid = static_cast<int>(blockIdx.x);
+  const int item = bid < nfull ? bid : nfull + (bid - nfull) / 2;
+  const bool has_b = bid < nfull;                 // this block runs Q block B too
+  const int pair = causal ? (npair - 1 - item / BH) : (item / BH);
+  const int bh = item % BH;
+  // Q tile of block A: the pair's first, or for a split item its own tile
+  const int qt_a = 2 * pair + (has_b ? 0 : (bid - nfull) & 1);
   const int bkv = bh / group;                   // key/value head of this query head
   // key tiles [lo, nt) needed by Q block A (tile 2*pair) and B (tile 2*pair + 1)
   const int ntA = causal ? min(2 * pair + 1, nkv) : nkv;
@@ -293,10 +302,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       prefetch_tmap(tmV);
       if constexpr (T::kStoreTma) prefetch_tmap(tmO);
       const uint32_t qf = ctx.bar(T::B_QFULL);
-      const int q0 = pair * 2 * BM;
-      mbar_arrive_expect_tx(qf, 2 * T::TILE);
+      const int q0 = qt_a * BM;
+      mbar_arrive_expect_tx(qf, (has_b ? 2 : 1) * T::TILE);
       T::load_rows(sbase + T::OFF_QA, tmQ, qf, q0, bh);
-      T::load_rows(sbase + T::OFF_QB, tmQ, qf, q0 + BM, bh);
+      if (has_b) T::load_rows(sbase + T::OFF_QB, tmQ, qf, q0 + BM, bh);
       bool ok = true;
       int cnt = 0;
       for (int j = loA; j < ntB && ok; ++j) {
@@ -334,7 +343,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         return ctx.wait(T::B_FULL + (2 * t + 1) % SLOTS, ((2 * t + 1) / SLOTS) & 1);
       };
       auto active_a = [&](int j) { return j < ntA; };
-      auto active_b = [&](int j) { return j >= loB; };
+      auto active_b = [&](int j) { return has_b && j >= loB; };
       bool ok = ctx.wait(T::B_QFULL, 0) && full_k(loA);
       if (ok) {
         tc_fence_after();
@@ -378,9 +387,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         if (j + 1 < ntB) {
           ok = k_next_ready || full_k(j + 1);
           if (!ok) break;
-          tc_fence_after();
-          T::issue_s(tmem + TM_S + 128, sbase + T::OFF_QB, sbase + T::OFF_SLOT + kslot_next * T::TILE);
-          mma_commit(ctx.bar(T::B_SFULL + 1));
+          if (has_b) {
+            tc_fence_after();
+            T::issue_s(tmem + TM_S + 128, sbase + T::OFF_QB,
+                       sbase + T::OFF_SLOT + kslot_next * T::TILE);
+            mma_commit(ctx.bar(T::B_SFULL + 1));
+          }
           mma_commit(ctx.bar(T::B_EMPTY + kslot_next));
         }
       }
@@ -391,10 +403,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     const int blk = warp >> 2;                    // 0: block A, 1: block B
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;             // row within the Q block
-    const int qt = 2 * pair + blk;                // Q tile index (128-row units)
+    const bool live = blk == 0 || has_b;          // block B idles in a split item
+    const int qt = qt_a + blk;                    // Q tile index (128-row units)
     const int q_row = qt * BM + row;
-    const int nt = blk ? ntB : ntA;
     const int lo = blk ? loB : loA;
+    const int nt = live ? (blk ? ntB : ntA) : lo;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * blk;
     const uint32_t o_addr = tmem + lane_addr + TM_O + 128 * blk;
@@ -528,7 +541,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       if (lane == 0) mbar_arrive(ctx.bar(T::B_PFULL + blk));
     }
 
-    if (ok && ctx.wait(T::B_ODONE + blk, 0)) {
+    if (ok && live && ctx.wait(T::B_ODONE + blk, 0)) {
       tc_fence_after();
       const float inv_l = out_scale / l;
       auto pack8 = [&](const uint32_t (&r)[32], int i) {
@@ -596,9 +609,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                 __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int BH, int N,
                 float scale_log2, int causal, int group, int window,
-                const float* __restrict__ alibi, int heads) {
+                const float* __restrict__ alibi, int heads, int nsplit) {
   fwd_body<Bf16, kWindow, kAlibi>(&tmQ, &tmK, &tmV, &tmO, O, LSE, BH, N, scale_log2, 1.f,
-                                  causal, group, window, alibi, heads);
+                                  causal, group, window, alibi, heads, nsplit);
 }
 
 // Q, K e4m3 [BH, N, 128]; tmV maps the transposed copy V^T [BH, 128, keys].
@@ -609,7 +622,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                float* __restrict__ LSE, int BH, int N, float scale_log2, float v_descale,
                int causal, int group, int window, const float* __restrict__ alibi, int heads) {
   fwd_body<Fp8, kWindow, kAlibi>(&tmQ, &tmK, &tmVt, nullptr, O, LSE, BH, N, scale_log2,
-                                 v_descale, causal, group, window, alibi, heads);
+                                 v_descale, causal, group, window, alibi, heads, 0);
 }
 
 // V [rows, 128] e4m3 -> V^T [128, ld] per head, 64 keys x 128 columns per
@@ -689,10 +702,23 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
   auto kernel = alibi ? (window > 0 ? fwd_bf16_kernel<true, true> : fwd_bf16_kernel<false, true>)
                       : (window > 0 ? fwd_bf16_kernel<true, false>
                                     : fwd_bf16_kernel<false, false>);
+  // Without the mask every item costs the same, so a last wave of r items on
+  // S SMs (r <= S/2) runs as 2r half-length blocks instead.
+  int nsplit = 0;
+  if (!causal) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        sms > 0) {
+      const long long items = static_cast<long long>(npair) * BH;
+      const long long r = items % sms;
+      if (items > sms && r > 0 && 2 * r <= sms) nsplit = static_cast<int>(r);
+    }
+  }
   if (ev.before) cudaEventRecord(ev.before, stream);
-  kernel<<<dim3(npair * BH), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
+  kernel<<<dim3(npair * BH + nsplit), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.o, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2,
-      causal, H / Hkv, window, alibi, H);
+      causal, H / Hkv, window, alibi, H, nsplit);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;

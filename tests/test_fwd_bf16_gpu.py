@@ -65,3 +65,24 @@ def test_bf16_long_causal_n8192_sampled():
     assert np.abs(np64(o[0, h]) - mean_prefix).max() <= O_MAX
 
 
+
+
+def test_bf16_forward_split_tail_items_ragged_gqa():
+    """Non-causal, 160 (Q pair, head) items on 152 SMs: the last 8 items run
+    as 16 one-tile blocks.  They are the last Q pair (tiles 18 and 19, the
+    second past N = 2500) of query heads 8..15; check those rows and others
+    against the oracle, and that nothing is written past O's end."""
+    B, Hq, Hkv, N, D = 1, 16, 4, 2500, 128
+    q, k, v = inputs.gqa_inputs(B, Hq, Hkv, N, D, torch.bfloat16, 77, "cuda")
+    scale = 1 / math.sqrt(D)
+    bo, o = guarded((B, Hq, N, D), torch.bfloat16)
+    bl, lse = guarded((B, Hq, N), torch.float32)
+    api.forward(q, k, v, causal=False, scale=scale, out=o, lse=lse)
+    rng = np.random.default_rng(77)
+    rows = np.unique(np.concatenate([np.arange(2304, N), rng.choice(2304, 64, replace=False)]))
+    for h in (0, 8, 11, 15):
+        t = h // (Hq // Hkv)
+        o_ref, lse_ref = orc.attention_forward_rows(np64(q[0, h, rows]), np64(k[0, t]),
+                                                    np64(v[0, t]), rows, scale, False)
+        assert_close_bf16(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, f"head {h}")
+    assert guards_intact(bo) and guards_intact(bl)
