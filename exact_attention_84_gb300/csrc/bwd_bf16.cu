@@ -10,7 +10,7 @@
 //   dV = P^T dO,  dS = P * (dO V^T - D),  dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels:
-//   bwd_pre      -D = -rowsum(dO * O) and -LSE * log2(e), padded per head
+//   bwd_pre      -scale D = -scale rowsum(dO * O) and -LSE * log2(e), padded per head
 //                to a multiple of 128 rows (so every block copy is aligned
 //                and in bounds), and zeroing of the fp32 dQ accumulator.
 //   bwd_main     one thread block per (b, h, 128-key block j).  K_j and V_j
@@ -21,13 +21,15 @@
 //                  dP^T = V_j dO_i^T  -> R1_X
 //                  softmax warps (key row = TMEM lane) form
 //                  P^T = exp2(S^T scale log2e - LSE log2e) and
-//                  dS^T = P^T (dP^T - D), write both as packed bf16 over the
+//                  dS^T = scale P^T (dP^T - D) (the softmax scale folded in
+//                  here, so dQ and dK need no later multiply), write both as
+//                  packed bf16 over the
 //                  R0_X columns they were computed from, and dS^T also to
 //                  shared memory (double-buffered);
 //                  dQ_i^T = K_j^T dS^T -> R1_X    (both operands MN-major)
 //                  dV += P^T dO_i, dK += dS^T Q_i  (A operand from TMEM)
 //                Block i's softmax overlaps the products of blocks i-1 and
-//                i+1; four writer warps add scale * dQ_i into the fp32
+//                i+1; four writer warps add dQ_i into the fp32
 //                accumulator with 16-byte vector atomics after a 4x4 register
 //                transpose (one warp instruction covers 4 rows x 128
 //                contiguous bytes).  dK and dV leave TMEM once.
@@ -134,14 +136,14 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------ bwd_pre
-// Sixteen threads per (padded) row, 16 bytes each: -D = -sum_k dO_k O_k and
+// Sixteen threads per (padded) row, 16 bytes each: -scale D = -scale sum_k dO_k O_k and
 // -LSE * log2(e), zero past the end of the sequence; the row of the dQ
 // accumulator is zeroed too.  The padded row count is a multiple of 128, so
 // every warp covers two whole rows and every shuffle has all 32 lanes.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       const float* __restrict__ lse,
-                                                      float* __restrict__ d_pad,
+                                                      float* __restrict__ d_pad, float scale,
                                                       float* __restrict__ lse_pad,
                                                       float* __restrict__ dq_acc, int N,
                                                       int Npad, size_t padded_rows) {
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (sub == 0) {            // stored negated: the main kernel only adds them
-    d_pad[prow] = -s;
+    d_pad[prow] = -s * scale;
     lse_pad[prow] = valid ? -lse[row] * kLog2e : 0.f;
   }
 }
@@ -479,10 +481,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         pk[e / 2 + 1] = pack_bf16x2(p2, p3);
         {
           float g0, g1, g2, g3;
-          f2unpack(f2mul(f2pack(p0, p1), f2add(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                               f2pack(d4.x, d4.y))), g0, g1);
-          f2unpack(f2mul(f2pack(p2, p3), f2add(f2pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
-                                               f2pack(d4.z, d4.w))), g2, g3);
+          // scale dS = P (scale dP - scale D), the staged value being -scale D
+          const uint64_t s2 = f2pack(scale, scale);
+          f2unpack(f2mul(f2pack(p0, p1), f2fma(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                               s2, f2pack(d4.x, d4.y))), g0, g1);
+          f2unpack(f2mul(f2pack(p2, p3), f2fma(f2pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                               s2, f2pack(d4.z, d4.w))), g2, g3);
           gk[e / 2] = pack_bf16x2(g0, g1);
           gk[e / 2 + 1] = pack_bf16x2(g2, g3);
         }
@@ -514,7 +518,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // drops the rows past N.
     if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
       tc_fence_after();
-      const float mul = sub == 0 ? 1.f : scale;
       const uint32_t src = tmem + lane_addr + (sub == 0 ? TM_DV : TM_DK);
       const uint32_t stage = sub == 0 ? OFF_V : OFF_K;
 #pragma unroll 1
@@ -525,10 +528,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<uint4*>(box + sw128_offset(row, (c & 1) * 4 + i)) = make_uint4(
-              pack_bf16x2(__uint_as_float(r[8 * i]) * mul, __uint_as_float(r[8 * i + 1]) * mul),
-              pack_bf16x2(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul),
-              pack_bf16x2(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul),
-              pack_bf16x2(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
+              pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+              pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+              pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+              pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -571,7 +574,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     quad * 32 + (lane & ~3);
 #pragma unroll
       for (int q0 = 0; q0 < BQ; q0 += 4) {
-        float v[4] = {g[q0] * scale, g[q0 + 1] * scale, g[q0 + 2] * scale, g[q0 + 3] * scale};
+        float v[4] = {g[q0], g[q0 + 1], g[q0 + 2], g[q0 + 3]};
         transpose4(v, lane);
         if (q0 + (lane & 3) < lim)
           red_add_v4(base + static_cast<size_t>(q0) * HD, v[0], v[1], v[2], v[3]);
@@ -592,7 +595,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // block per (query head, 128-query block i), K_j / V_j streamed in 64-key
 // tiles in increasing key order, dQ_i accumulated in TMEM and written once:
 //   S = Q_i K_j^T, dP = dO_i V_j^T            (shared-memory operands)
-//   P = exp2(S scale log2e - LSE log2e [- ALiBi]),  dS = P * (dP - D)
+//   P = exp2(S scale log2e - LSE log2e [- ALiBi]),  dS = scale P * (dP - D)
 //   dQ_i += dS K_j                             (dS from TMEM, K_j MN-major)
 // Two TMEM buffers of [S | dP] let the softmax of tile t overlap the
 // products of tiles t-1 and t+1.  Each dQ element is summed by one thread
@@ -775,7 +778,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const bool row_valid = q < N;
     const size_t srow = static_cast<size_t>(bh) * Npad + q;      // q < Npad always
     const float nlse = lse_pad[srow];                            // -LSE log2e
-    const float nd = d_pad[srow];                                // -D
+    const float nd = d_pad[srow];                                // -scale D
     const float scale_log2 = scale * kLog2e;
     const float slope_log2 = kAlibi ? alibi[bh % heads] * kLog2e : 0.f;
     // keys this row sees: [lo, hi]
@@ -812,8 +815,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           p0 = v0 ? p0 : 0.f;
           p1 = v1 ? p1 : 0.f;
         }
-        gk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) + nd),
-                                p1 * (__uint_as_float(dr[e + 1]) + nd));
+        gk[e / 2] = pack_bf16x2(p0 * fmaf(__uint_as_float(dr[e]), scale, nd),
+                                p1 * fmaf(__uint_as_float(dr[e + 1]), scale, nd));
       }
       // packed dS over the first 16 of the 32 columns this thread just read
       tmem_st16(s_addr, gk);
@@ -834,10 +837,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             d4[i] = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
-                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
-                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
-                pack_bf16x2(__uint_as_float(r[8 * i + 6]) * scale, __uint_as_float(r[8 * i + 7]) * scale));
+                pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
         }
       }
     }
@@ -901,7 +904,7 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   const bool deterministic = dq_maps != nullptr;
   bwd_pre_kernel<<<dim3(static_cast<unsigned>((prows + 15) / 16)), dim3(256), 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, d_pad,
-      lse_pad, deterministic ? nullptr : dq_acc, N, Npad, prows);
+      scale, lse_pad, deterministic ? nullptr : dq_acc, N, Npad, prows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int nkv = (N + BKV - 1) / BKV;
