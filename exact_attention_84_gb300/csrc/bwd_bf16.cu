@@ -30,9 +30,9 @@
 //                  dV += P^T dO_i, dK += dS^T Q_i  (A operand from TMEM)
 //                Block i's softmax overlaps the products of blocks i-1 and
 //                i+1; four writer warps add dQ_i into the fp32
-//                accumulator with 16-byte vector atomics after a 4x4 register
-//                transpose (one warp instruction covers 4 rows x 128
-//                contiguous bytes).  dK and dV leave TMEM once.
+//                accumulator with fp32 atomics (one warp instruction covers
+//                one query row's 128 contiguous bytes of its quadrant).  dK
+//                and dV leave TMEM once.
 //   bwd_convert  dQ = bf16(accumulator).
 // Causal: query blocks entirely above the key block are skipped; the blocks
 // that straddle the diagonal are masked element-wise.
@@ -108,23 +108,9 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
   return base + OFF_BAR + 8u * static_cast<uint32_t>(i);
 }
 
-// Four consecutive fp32 values added atomically (16-byte aligned address).
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-               ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
-
-// 4x4 transpose across each group of four lanes: on entry lane l holds
-// x[c] = its own value at position c; on exit it holds x[c] = the value that
-// lane (l & ~3) + c held at position (l & 3).
-__device__ __forceinline__ void transpose4(float (&x)[4], int lane) {
-  const bool hi2 = lane & 2, hi1 = lane & 1;
-  float r0 = __shfl_xor_sync(0xffffffffu, hi2 ? x[0] : x[2], 2);
-  float r1 = __shfl_xor_sync(0xffffffffu, hi2 ? x[1] : x[3], 2);
-  if (hi2) { x[0] = r0; x[1] = r1; } else { x[2] = r0; x[3] = r1; }
-  r0 = __shfl_xor_sync(0xffffffffu, hi1 ? x[0] : x[1], 1);
-  r1 = __shfl_xor_sync(0xffffffffu, hi1 ? x[2] : x[3], 1);
-  if (hi1) { x[0] = r0; x[2] = r1; } else { x[1] = r0; x[3] = r1; }
+// One fp32 value added atomically (the result is not needed).
+__device__ __forceinline__ void red_add(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 struct Ctx {
@@ -566,19 +552,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(sbase, B_DQFREE + x));
-      // Per group of 4 queries, transpose within each 4-lane group so that a
-      // lane holds 4 consecutive head-dimension values of one query row:
-      // one warp instruction then adds 4 rows x 128 contiguous bytes.
+      // Lane = head-dimension entry, so one warp instruction adds a query
+      // row's 32 entries of this quadrant: 128 contiguous bytes, no shuffles
+      // (fewer issue slots taken beside the MMA-issuing warp than the 4x4
+      // register transpose that 16-byte vector atomics need).
       const int lim = min(BQ, N - qb);
-      float* base = dq_acc + (static_cast<size_t>(bh) * N + qb + (lane & 3)) * HD +
-                    quad * 32 + (lane & ~3);
+      float* base = dq_acc + (static_cast<size_t>(bh) * N + qb) * HD + quad * 32 + lane;
 #pragma unroll
-      for (int q0 = 0; q0 < BQ; q0 += 4) {
-        float v[4] = {g[q0], g[q0 + 1], g[q0 + 2], g[q0 + 3]};
-        transpose4(v, lane);
-        if (q0 + (lane & 3) < lim)
-          red_add_v4(base + static_cast<size_t>(q0) * HD, v[0], v[1], v[2], v[3]);
-      }
+      for (int q = 0; q < BQ; ++q)
+        if (q < lim) red_add(base + static_cast<size_t>(q) * HD, g[q]);
     }
   }
 
