@@ -94,10 +94,10 @@ constexpr uint32_t TM_DV = 256, TM_DK = 384;
 constexpr int NTHREADS = 448;   // 0-7 softmax, 8-11 dQ writers, 12 producer, 13 MMA
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
-// Query heads whose thread blocks are ordered together: up to 32, as many as
-// keep their Q, dO (bf16) and fp32 dQ accumulator rows (1 KiB per query row)
-// within ~128 MB of L2, and at least 8.
-constexpr int kHeadGroupMax = 32, kHeadGroupMin = 8;
+// Key/value heads whose thread blocks are ordered together: 8, fewer when
+// the query rows they serve (Q, dO and the fp32 dQ accumulator: 1 KiB per
+// row, g query heads per key/value head) pass ~128 MB of L2.
+constexpr int kHeadGroupKv = 8;
 constexpr long long kHeadGroupBytes = 128ll << 20;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -897,13 +897,12 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   if (ev.before) cudaEventRecord(ev.before, stream);
   const int g = H / Hkv;
   // Blocks go heavy-first (increasing key block) within each group of heads:
-  // a larger group is a longer heavy-first list, which evens out the end of
-  // the grid (grouped heads make each block g times longer, where it counts
-  // most), while the group's rows must stay in L2.
-  long long fit = kHeadGroupBytes / (static_cast<long long>(N) * 1024);
-  fit = fit < kHeadGroupMin ? kHeadGroupMin : (fit > kHeadGroupMax ? kHeadGroupMax : fit);
-  const int hq_group = static_cast<int>(fit);
-  const int head_group = max(1, hq_group / g);   // key/value heads per group
+  // a longer heavy-first list evens out the end of the grid (grouped query
+  // heads make each block g times longer, where it counts most), while the
+  // group's rows must stay in L2.
+  long long fit = kHeadGroupBytes / (static_cast<long long>(g) * N * 1024);
+  fit = fit < 1 ? 1 : (fit > kHeadGroupKv ? kHeadGroupKv : fit);
+  const int head_group = static_cast<int>(fit);   // key/value heads per group
   auto kernel = deterministic
                     ? (alibi ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>)
                     : (alibi ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>);
