@@ -444,11 +444,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
         if constexpr (kAlibi) {
           // exponent offset -LSE log2e - slope |i - j| log2e per query column
-          const float de = d0 + static_cast<float>(e);
-          l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
-          l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
-          l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
-          l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
+          if (causal) {
+            // every key the mask leaves has key <= query, so |i - j| = i - j:
+            // no absolute value, and the offsets on packed pairs
+            const uint64_t ns2 = f2pack(-slope_log2, -slope_log2);
+            const uint64_t d02 = f2pack(d0, d0);
+            const uint64_t de01 = f2add(d02, f2pack(static_cast<float>(e), static_cast<float>(e + 1)));
+            const uint64_t de23 = f2add(d02, f2pack(static_cast<float>(e + 2), static_cast<float>(e + 3)));
+            f2unpack(f2fma(ns2, de01, f2pack(l4.x, l4.y)), l4.x, l4.y);
+            f2unpack(f2fma(ns2, de23, f2pack(l4.z, l4.w)), l4.z, l4.w);
+          } else {
+            const float de = d0 + static_cast<float>(e);
+            l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
+            l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
+            l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
+            l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
+          }
         }
         // exponent arguments and dS = P (dP - D) on packed fp32 pairs
         const uint64_t sc2 = f2pack(scale_log2, scale_log2);
