@@ -81,7 +81,8 @@ constexpr int B_SFULL = B_QEMPTY + STAGES; // + buffer: S^T and dP^T in TMEM
 constexpr int B_PFULL = B_SFULL + 2;       // + buffer: P^T, dS^T written (8 warps)
 constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
 constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
-constexpr int B_DONE = B_DQFREE + 2;       // every product of the block completed
+constexpr int B_DKV = B_DQFREE + 2;       // + buffer: dV/dK(i) have read R0_X
+constexpr int B_DONE = B_DKV + 2;          // every product of the block completed
 constexpr int B_EPI = B_DONE + 1;          // + (0 dV, 1 dK): staged in shared memory (4 warps)
 constexpr int NBAR = B_EPI + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -91,9 +92,11 @@ constexpr uint32_t TMEM_COLS = 512;
 // buffer X: R0 = [128 X, 128 X + 64), R1 = [128 X + 64, 128 X + 128)
 constexpr uint32_t TM_DV = 256, TM_DK = 384;
 
-constexpr int NTHREADS = 448;   // 0-7 softmax, 8-11 dQ writers, 12 producer, 13 MMA
+// 0-7 softmax, 8-11 dQ writers, 12 producer, 13 gradient products, 14 score products
+constexpr int NTHREADS = 480;
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
+constexpr int WARP_MMA2 = 14;
 // Key/value heads whose thread blocks are ordered together: 8, fewer when
 // the query rows they serve (Q, dO and the fp32 dQ accumulator: 1 KiB per
 // row, g query heads per key/value head) pass ~128 MB of L2.
@@ -248,6 +251,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_PFULL + x), 8);
       mbar_init(bar_addr(sbase, B_DQFULL + x), 1);
       mbar_init(bar_addr(sbase, B_DQFREE + x), 4);
+      mbar_init(bar_addr(sbase, B_DKV + x), 1);
     }
     mbar_init(bar_addr(sbase, B_DONE), 1);
     mbar_init(bar_addr(sbase, B_EPI + 0), 4);
@@ -299,21 +303,74 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == WARP_MMA) {
-    // ------------------------------------------------------------ MMA issuer
-    // Order, per query block i in buffer X = i mod 2:
-    //   [P(i) ready] dQ^T(i) dV(i) dK(i) | S^T(i+2) [dQ^T(i) drained] dP^T(i+2)
-    // so block i+1's softmax overlaps block i's gradient products and block
-    // i+2's score products, and the writers drain dQ^T(i) meanwhile.
+    // ------------------------------------------------------- gradient issuer
+    // Per query block i in buffer X = i mod 2, once its softmax is done:
+    //   dV(i) dK(i) [DKV(X): R0_X read] dQ^T(i) [DQFULL(X)]
+    // The score products come from a second issuing warp on another SM
+    // sub-partition: one thread issuing every product shares its
+    // sub-partition's issue slots with the softmax and writer warps there,
+    // and loses most of its rate while they are busy.
+    if (lane == 0) {
+      auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
+      const uint64_t kd_mn = sdesc_sw128(sbase + OFF_K, HALF, 1024);   // K_j^T, MN-major (dQ^T)
+      bool ok = ctx.wait(B_KVFULL, 0);
+      for (int it = 0; it < nit && ok; ++it) {
+        const int x = it & 1;
+        const uint32_t sb = stage(it);
+        const uint32_t r0 = tmem + 128u * x, r1 = tmem + 128u * x + 64u;
+        if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
+        tc_fence_after();
+        // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
+        // P^T packed in columns [32g, 32g+16) and dS^T in [32g+16, 32g+32);
+        // 16 queries = 8 packed columns.
+        {
+          const uint64_t dod = sdesc_sw128(sb + ST_DO, QHALF, 1024);   // dO_i, MN-major
+          const uint64_t qd = sdesc_sw128(sb + ST_Q, QHALF, 1024);     // Q_i, MN-major
+          uint32_t ap[4], as[4];
+          uint64_t bo[4], bq[4];
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            ap[kk] = r0 + 32 * (kk >> 1) + 8 * (kk & 1);
+            as[kk] = ap[kk] + 16;
+            bo[kk] = dod + ((kk * 2048) >> 4);
+            bq[kk] = qd + ((kk * 2048) >> 4);
+          }
+          const uint32_t acc = it > 0 ? 1u : 0u;
+          mma_ts_batch4(tmem + TM_DV, ap, bo, IDESC_DKV, acc);
+          mma_ts_batch4(tmem + TM_DK, as, bq, IDESC_DKV, acc);
+        }
+        mma_commit(bar_addr(sbase, B_DKV + x));
+        mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
+        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
+        if constexpr (kDq) {
+          const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            a[kk] = kd_mn + ((kk * 2048) >> 4);
+            b[kk] = dsd + ((kk * 2048) >> 4);
+          }
+          mma_ss_batch8(r1, a, b, IDESC_DQ, 0u);
+          mma_commit(bar_addr(sbase, B_DQFULL + x));
+        }
+      }
+      // The score products all completed before the last softmax, so this
+      // commit covers every product of the block.
+      if (ok) mma_commit(bar_addr(sbase, B_DONE));
+    }
+    __syncwarp();
+  } else if (warp == WARP_MMA2) {
+    // ---------------------------------------------------------- score issuer
+    // S^T(i) and dP^T(i) into buffer X = i mod 2, for i = 0, 1 at once and
+    // then i + 2 as soon as dV/dK(i) have read R0_X (DKV) and the writers
+    // have drained dQ^T(i) from R1_X (DQFREE).
     if (lane == 0) {
       const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V;
       auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
-      auto r0 = [&](int it) { return tmem + 128u * (it & 1); };
-      auto r1 = [&](int it) { return tmem + 128u * (it & 1) + 64u; };
       // Descriptors of the key-block operands, fixed for the whole block; a
       // k-step advances the start-address field (units of 16 bytes).
       const uint64_t kd_k = sdesc_sw128(kA, 16, 1024);        // K_j, K-major (S^T)
       const uint64_t vd_k = sdesc_sw128(vA, 16, 1024);        // V_j, K-major (dP^T)
-      const uint64_t kd_mn = sdesc_sw128(kA, HALF, 1024);     // K_j^T, MN-major (dQ^T)
       // S^T (into R0) or dP^T (into R1): reduction over d.
       auto issue_sdp = [&](int it, bool dp) {
         const uint64_t ad = dp ? vd_k : kd_k;
@@ -324,7 +381,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           a[kk] = ad + (((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
           b[kk] = bd + (((kk >> 2) * QHALF + (kk & 3) * 32) >> 4);
         }
-        mma_ss_batch8(dp ? r1(it) : r0(it), a, b, IDESC_ST, 0u);
+        mma_ss_batch8(tmem + 128u * (it & 1) + (dp ? 64u : 0u), a, b, IDESC_ST, 0u);
       };
       auto wait_q = [&](int it) {
         return ctx.wait(B_QFULL + it % STAGES, (it / STAGES) & 1);
@@ -337,58 +394,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         issue_sdp(it, true);
         mma_commit(bar_addr(sbase, B_SFULL + (it & 1)));
       }
-      for (int it = 0; it < nit && ok; ++it) {
+      for (int it = 0; it + 2 < nit && ok; ++it) {
         const int x = it & 1;
-        const uint32_t sb = stage(it);
-        if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
+        if (!(ok = ctx.wait(B_DKV + x, (it >> 1) & 1) && wait_q(it + 2))) break;
         tc_fence_after();
-        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
+        issue_sdp(it + 2, false);
         if constexpr (kDq) {
-          const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
-          uint64_t a[8], b[8];
-#pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk) {
-            a[kk] = kd_mn + ((kk * 2048) >> 4);
-            b[kk] = dsd + ((kk * 2048) >> 4);
-          }
-          mma_ss_batch8(r1(it), a, b, IDESC_DQ, 0u);
-          mma_commit(bar_addr(sbase, B_DQFULL + x));
-        }
-        // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
-        // P^T packed in columns [32g, 32g+16) and dS^T in [32g+16, 32g+32);
-        // 16 queries = 8 packed columns.
-        {
-          const uint64_t dod = sdesc_sw128(sb + ST_DO, QHALF, 1024);   // dO_i, MN-major
-          const uint64_t qd = sdesc_sw128(sb + ST_Q, QHALF, 1024);     // Q_i, MN-major
-          uint32_t ap[4], as[4];
-          uint64_t bo[4], bq[4];
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {
-            ap[kk] = r0(it) + 32 * (kk >> 1) + 8 * (kk & 1);
-            as[kk] = ap[kk] + 16;
-            bo[kk] = dod + ((kk * 2048) >> 4);
-            bq[kk] = qd + ((kk * 2048) >> 4);
-          }
-          const uint32_t acc = it > 0 ? 1u : 0u;
-          mma_ts_batch4(tmem + TM_DV, ap, bo, IDESC_DKV, acc);
-          mma_ts_batch4(tmem + TM_DK, as, bq, IDESC_DKV, acc);
-        }
-        mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
-        if (it + 2 < nit) {
-          // R0_X was read by dV/dK(i) (issued above, executed in order).
-          if (!(ok = wait_q(it + 2))) break;
+          if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
           tc_fence_after();
-          issue_sdp(it + 2, false);
-          // R1_X holds dQ^T(i) until the writers have read it.
-          if constexpr (kDq) {
-            if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
-            tc_fence_after();
-          }
-          issue_sdp(it + 2, true);
-          mma_commit(bar_addr(sbase, B_SFULL + x));
         }
+        issue_sdp(it + 2, true);
+        mma_commit(bar_addr(sbase, B_SFULL + x));
       }
-      if (ok) mma_commit(bar_addr(sbase, B_DONE));
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -545,7 +562,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bulk_wait_group_read0();   // the block may exit once the tiles have been read
       }
     }
-  } else if (kDq) {
+  } else if (kDq && warp < WARP_TMA) {
     // ------------------------------------------------------------ dQ writers
     const int quad = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
