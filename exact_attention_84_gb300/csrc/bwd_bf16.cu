@@ -29,7 +29,10 @@
 //                  dQ_i^T = K_j^T dS^T -> R1_X    (both operands MN-major)
 //                  dV += P^T dO_i, dK += dS^T Q_i  (A operand from TMEM)
 //                Block i's softmax overlaps the products of blocks i-1 and
-//                i+1; four writer warps add dQ_i into the fp32
+//                i+1.  Three warps issue the products, each on its own SM
+//                sub-partition (S^T/dP^T, dV/dK, dQ^T), so the issue slots
+//                that the softmax and writer warps take on one do not stall
+//                the others.  Four writer warps add dQ_i into the fp32
 //                accumulator with fp32 atomics (one warp instruction covers
 //                one query row's 128 contiguous bytes of its quadrant).  dK
 //                and dV leave TMEM once.
@@ -82,8 +85,9 @@ constexpr int B_PFULL = B_SFULL + 2;       // + buffer: P^T, dS^T written (8 war
 constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
 constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
 constexpr int B_DKV = B_DQFREE + 2;       // + buffer: dV/dK(i) have read R0_X
-constexpr int B_DONE = B_DKV + 2;          // every product of the block completed
-constexpr int B_EPI = B_DONE + 1;          // + (0 dV, 1 dK): staged in shared memory (4 warps)
+constexpr int B_DONE = B_DKV + 2;          // the dV/dK issuer's products completed
+constexpr int B_DONE3 = B_DONE + 1;        // dQ issuer's products completed
+constexpr int B_EPI = B_DONE3 + 1;          // + (0 dV, 1 dK): staged in shared memory (4 warps)
 constexpr int NBAR = B_EPI + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;   // base is 1024-aligned (checked)
@@ -92,11 +96,12 @@ constexpr uint32_t TMEM_COLS = 512;
 // buffer X: R0 = [128 X, 128 X + 64), R1 = [128 X + 64, 128 X + 128)
 constexpr uint32_t TM_DV = 256, TM_DK = 384;
 
-// 0-7 softmax, 8-11 dQ writers, 12 producer, 13 gradient products, 14 score products
-constexpr int NTHREADS = 480;
+// 0-7 softmax, 8-11 dQ writers, 12 producer; MMA issuers: 13 dV/dK, 14 S^T/dP^T, 15 dQ^T
+constexpr int NTHREADS = 512;
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
 constexpr int WARP_MMA2 = 14;
+constexpr int WARP_MMA3 = 15;
 // Key/value heads whose thread blocks are ordered together: 8, fewer when
 // the query rows they serve (Q, dO and the fp32 dQ accumulator: 1 KiB per
 // row, g query heads per key/value head) pass ~128 MB of L2.
@@ -254,6 +259,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_DKV + x), 1);
     }
     mbar_init(bar_addr(sbase, B_DONE), 1);
+    mbar_init(bar_addr(sbase, B_DONE3), 1);
     mbar_init(bar_addr(sbase, B_EPI + 0), 4);
     mbar_init(bar_addr(sbase, B_EPI + 1), 4);
     *abort_flag = 0;
@@ -305,19 +311,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------- gradient issuer
     // Per query block i in buffer X = i mod 2, once its softmax is done:
-    //   dV(i) dK(i) [DKV(X): R0_X read] dQ^T(i) [DQFULL(X)]
-    // The score products come from a second issuing warp on another SM
-    // sub-partition: one thread issuing every product shares its
+    //   dV(i) dK(i) [DKV(X): R0_X read]
+    // The score products and dQ^T come from two more issuing warps, each on
+    // its own SM sub-partition: one thread issuing every product shares its
     // sub-partition's issue slots with the softmax and writer warps there,
     // and loses most of its rate while they are busy.
     if (lane == 0) {
       auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
-      const uint64_t kd_mn = sdesc_sw128(sbase + OFF_K, HALF, 1024);   // K_j^T, MN-major (dQ^T)
       bool ok = ctx.wait(B_KVFULL, 0);
       for (int it = 0; it < nit && ok; ++it) {
         const int x = it & 1;
         const uint32_t sb = stage(it);
-        const uint32_t r0 = tmem + 128u * x, r1 = tmem + 128u * x + 64u;
+        const uint32_t r0 = tmem + 128u * x;
         if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
         tc_fence_after();
         // dV += P^T dO_i, dK += dS^T Q_i.  R0_X holds, per 32-query slice g,
@@ -341,22 +346,34 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mma_commit(bar_addr(sbase, B_DKV + x));
         mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
-        // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X.
-        if constexpr (kDq) {
-          const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
-          uint64_t a[8], b[8];
-#pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk) {
-            a[kk] = kd_mn + ((kk * 2048) >> 4);
-            b[kk] = dsd + ((kk * 2048) >> 4);
-          }
-          mma_ss_batch8(r1, a, b, IDESC_DQ, 0u);
-          mma_commit(bar_addr(sbase, B_DQFULL + x));
-        }
       }
       // The score products all completed before the last softmax, so this
-      // commit covers every product of the block.
+      // commit covers every product but dQ^T (B_DONE3).
       if (ok) mma_commit(bar_addr(sbase, B_DONE));
+    }
+    __syncwarp();
+  } else if (kDq && warp == WARP_MMA3) {
+    // ------------------------------------------------------------ dQ issuer
+    // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X, whose
+    // dP^T(i) the softmax has read, once P(i) is ready.
+    if (lane == 0) {
+      const uint64_t kd_mn = sdesc_sw128(sbase + OFF_K, HALF, 1024);   // K_j^T, MN-major
+      bool ok = ctx.wait(B_KVFULL, 0);
+      for (int it = 0; it < nit && ok; ++it) {
+        const int x = it & 1;
+        if (!(ok = ctx.wait(B_PFULL + x, (it >> 1) & 1))) break;
+        tc_fence_after();
+        const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
+        uint64_t a[8], b[8];
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          a[kk] = kd_mn + ((kk * 2048) >> 4);
+          b[kk] = dsd + ((kk * 2048) >> 4);
+        }
+        mma_ss_batch8(tmem + 128u * x + 64u, a, b, IDESC_DQ, 0u);
+        mma_commit(bar_addr(sbase, B_DQFULL + x));
+      }
+      if (ok) mma_commit(bar_addr(sbase, B_DONE3));
     }
     __syncwarp();
   } else if (warp == WARP_MMA2) {
@@ -534,7 +551,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // staged over the tile it belongs to (dV over V_j, dK over K_j) in the
     // same swizzled boxes and leaves with one bulk tensor store, which also
     // drops the rows past N.
-    if (ok && nit > 0 && ctx.wait(B_DONE, 0)) {
+    if (ok && nit > 0 && ctx.wait(B_DONE, 0) && (!kDq || ctx.wait(B_DONE3, 0))) {
       tc_fence_after();
       const uint32_t src = tmem + lane_addr + (sub == 0 ? TM_DV : TM_DK);
       const uint32_t stage = sub == 0 ? OFF_V : OFF_K;
