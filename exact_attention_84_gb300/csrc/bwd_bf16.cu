@@ -648,11 +648,12 @@ constexpr int DQB_FULL = 1;                          // + stage
 constexpr int DQB_EMPTY = DQB_FULL + DQ_STAGES;      // + stage
 constexpr int DQB_SFULL = DQB_EMPTY + DQ_STAGES;     // + buffer
 constexpr int DQB_PFULL = DQB_SFULL + 2;             // + buffer (8 warps)
-constexpr int DQB_DONE = DQB_PFULL + 2;
+constexpr int DQB_DSREAD = DQB_PFULL + 2;            // + buffer: dQ(t) has read dS(t)
+constexpr int DQB_DONE = DQB_DSREAD + 2;
 constexpr int DQ_NBAR = DQB_DONE + 1;
 constexpr uint32_t DQ_OFF_MISC = DQ_OFF_BAR + DQ_NBAR * 8;
 constexpr uint32_t DQ_SMEM = DQ_OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
-constexpr int DQ_THREADS = 320;                // 0-7 softmax, 8 producer, 9 MMA
+constexpr int DQ_THREADS = 352;                // 0-7 softmax, 8 producer, 9-10 MMA issuers
 constexpr uint32_t DQ_TM_DQ = 256;             // buffer x: S at 128x, dP at 128x + 64
 constexpr uint32_t IDESC_DQ_S = idesc_bf16(DQ_BQ, DQ_BK, false, false);
 constexpr uint32_t IDESC_DQ_ACC = idesc_bf16(DQ_BQ, HD, false, true);
@@ -697,6 +698,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(DQB_SFULL + x), 1);
       mbar_init(bar(DQB_PFULL + x), 8);
+      mbar_init(bar(DQB_DSREAD + x), 1);
     }
     mbar_init(bar(DQB_DONE), 1);
     *abort_flag = 0;
@@ -739,7 +741,41 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------- dQ issuer
+    // dQ += dS K_t once the softmax of tile t is done; the score products
+    // come from warp 10 on another SM sub-partition (one thread issuing all
+    // of them shares its sub-partition's issue slots with two softmax warps).
+    if (lane == 0) {
+      auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
+      bool ok = true;
+      for (int t = 0; t < nt && ok; ++t) {
+        const int x = t & 1;
+        if (!(ok = wait(DQB_PFULL + x, (t >> 1) & 1))) break;
+        tc_fence_after();
+        // dQ += dS K_t: dS packed in TMEM (keys 0-31 in columns [0, 16),
+        // keys 32-63 in [32, 48) of the buffer), K_t MN-major (16 keys =
+        // 2048 bytes per step, 64-column blocks 8 KiB apart).
+        {
+          const uint64_t kd = sdesc_sw128(ring(t), DQ_KHALF, 1024);
+          uint32_t a[4];
+          uint64_t b[4];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            a[kk] = tmem + 128u * x + 32 * (kk >> 1) + 8 * (kk & 1);
+            b[kk] = kd + ((kk * 2048) >> 4);
+          }
+          mma_ts_batch4(tmem + DQ_TM_DQ, a, b, IDESC_DQ_ACC, t > 0 ? 1u : 0u);
+        }
+        // S(t), dP(t) completed before the softmax of tile t, so this covers
+        // every reader of stage t and of buffer x's dS.
+        mma_commit(bar(DQB_EMPTY + t % DQ_STAGES));
+        mma_commit(bar(DQB_DSREAD + x));
+      }
+      if (ok) mma_commit(bar(DQB_DONE));
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------- score issuer
     if (lane == 0) {
       auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
       auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
@@ -764,39 +800,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mma_ss_batch8(buf + 64, a2, b2, IDESC_DQ_S, 0u);
       };
       bool ok = wait(DQB_QFULL, 0);
-      for (int t = 0; t < 2 && t < nt && ok; ++t) {
+      for (int t = 0; t < nt && ok; ++t) {
+        // buffer t & 1 holds dS(t - 2) until dQ(t - 2) has read it
+        if (t >= 2 && !(ok = wait(DQB_DSREAD + (t & 1), ((t - 2) >> 1) & 1))) break;
         if (!(ok = full(t))) break;
         tc_fence_after();
         issue_sdp(t);
-        mma_commit(bar(DQB_SFULL + t));
+        mma_commit(bar(DQB_SFULL + (t & 1)));
       }
-      for (int t = 0; t < nt && ok; ++t) {
-        const int x = t & 1;
-        if (!(ok = wait(DQB_PFULL + x, (t >> 1) & 1))) break;
-        tc_fence_after();
-        // dQ += dS K_t: dS packed in TMEM (keys 0-31 in columns [0, 16),
-        // keys 32-63 in [32, 48) of the buffer), K_t MN-major (16 keys =
-        // 2048 bytes per step, 64-column blocks 8 KiB apart).
-        {
-          const uint64_t kd = sdesc_sw128(ring(t), DQ_KHALF, 1024);
-          uint32_t a[4];
-          uint64_t b[4];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            a[kk] = tmem + 128u * x + 32 * (kk >> 1) + 8 * (kk & 1);
-            b[kk] = kd + ((kk * 2048) >> 4);
-          }
-          mma_ts_batch4(tmem + DQ_TM_DQ, a, b, IDESC_DQ_ACC, t > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(DQB_EMPTY + t % DQ_STAGES));
-        if (t + 2 < nt) {
-          if (!(ok = full(t + 2))) break;
-          tc_fence_after();
-          issue_sdp(t + 2);           // after dQ(t) has read dS(t) (in issue order)
-          mma_commit(bar(DQB_SFULL + x));
-        }
-      }
-      if (ok) mma_commit(bar(DQB_DONE));
     }
     __syncwarp();
   } else {
