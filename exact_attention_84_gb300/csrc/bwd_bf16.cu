@@ -346,13 +346,27 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mma_commit(bar_addr(sbase, B_DKV + x));
         mma_commit(bar_addr(sbase, B_QEMPTY + it % STAGES));
+        // With the ALiBi bias the softmax warps are busier and a third
+        // issuer beside them measured slower: dQ^T comes from here then.
+        if constexpr (kDq && kAlibi) {
+          const uint64_t kd_mn = sdesc_sw128(sbase + OFF_K, HALF, 1024);   // K_j^T, MN-major
+          const uint64_t dsd = sdesc_sw128(sbase + OFF_DS + x * DS_TILE, DS_TILE, 1024);
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            a[kk] = kd_mn + ((kk * 2048) >> 4);
+            b[kk] = dsd + ((kk * 2048) >> 4);
+          }
+          mma_ss_batch8(tmem + 128u * x + 64u, a, b, IDESC_DQ, 0u);
+          mma_commit(bar_addr(sbase, B_DQFULL + x));
+        }
       }
       // The score products all completed before the last softmax, so this
       // commit covers every product but dQ^T (B_DONE3).
       if (ok) mma_commit(bar_addr(sbase, B_DONE));
     }
     __syncwarp();
-  } else if (kDq && warp == WARP_MMA3) {
+  } else if (kDq && !kAlibi && warp == WARP_MMA3) {
     // ------------------------------------------------------------ dQ issuer
     // dQ_i^T = K_j^T dS^T (reduction over the 128 keys) into R1_X, whose
     // dP^T(i) the softmax has read, once P(i) is ready.
@@ -551,7 +565,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // staged over the tile it belongs to (dV over V_j, dK over K_j) in the
     // same swizzled boxes and leaves with one bulk tensor store, which also
     // drops the rows past N.
-    if (ok && nit > 0 && ctx.wait(B_DONE, 0) && (!kDq || ctx.wait(B_DONE3, 0))) {
+    if (ok && nit > 0 && ctx.wait(B_DONE, 0) && (!kDq || kAlibi || ctx.wait(B_DONE3, 0))) {
       tc_fence_after();
       const uint32_t src = tmem + lane_addr + (sub == 0 ? TM_DV : TM_DK);
       const uint32_t stage = sub == 0 ? OFF_V : OFF_K;
