@@ -80,8 +80,9 @@ constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_TILE;
 constexpr int B_KVFULL = 0;
 constexpr int B_QFULL = 1;                 // + stage
 constexpr int B_QEMPTY = B_QFULL + STAGES; // + stage
-constexpr int B_SFULL = B_QEMPTY + STAGES; // + buffer: S^T and dP^T in TMEM
-constexpr int B_PFULL = B_SFULL + 2;       // + buffer: P^T, dS^T written (8 warps)
+constexpr int B_SFULL = B_QEMPTY + STAGES; // + buffer: S^T in TMEM
+constexpr int B_DPFULL = B_SFULL + 2;      // + buffer: dP^T in TMEM
+constexpr int B_PFULL = B_DPFULL + 2;      // + buffer: P^T, dS^T written (8 warps)
 constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
 constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
 constexpr int B_DKV = B_DQFREE + 2;       // + buffer: dV/dK(i) have read R0_X
@@ -253,6 +254,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar_addr(sbase, B_SFULL + x), 1);
+      mbar_init(bar_addr(sbase, B_DPFULL + x), 1);
       mbar_init(bar_addr(sbase, B_PFULL + x), 8);
       mbar_init(bar_addr(sbase, B_DQFULL + x), 1);
       mbar_init(bar_addr(sbase, B_DQFREE + x), 4);
@@ -393,8 +395,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == WARP_MMA2) {
     // ---------------------------------------------------------- score issuer
     // S^T(i) and dP^T(i) into buffer X = i mod 2, for i = 0, 1 at once and
-    // then i + 2 as soon as dV/dK(i) have read R0_X (DKV) and the writers
-    // have drained dQ^T(i) from R1_X (DQFREE).
+    // then i + 2: S^T as soon as dV/dK(i) have read R0_X (DKV), dP^T once
+    // the writers have drained dQ^T(i) from R1_X (DQFREE).  Each has its own
+    // barrier, so the softmax takes the exponentials while dP^T is still on
+    // its way.
     if (lane == 0) {
       const uint32_t kA = sbase + OFF_K, vA = sbase + OFF_V;
       auto stage = [&](int it) { return sbase + OFF_STAGE + (it % STAGES) * STAGE_BYTES; };
@@ -422,20 +426,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!(ok = wait_q(it))) break;
         tc_fence_after();
         issue_sdp(it, false);
-        issue_sdp(it, true);
         mma_commit(bar_addr(sbase, B_SFULL + (it & 1)));
+        issue_sdp(it, true);
+        mma_commit(bar_addr(sbase, B_DPFULL + (it & 1)));
       }
       for (int it = 0; it + 2 < nit && ok; ++it) {
         const int x = it & 1;
         if (!(ok = ctx.wait(B_DKV + x, (it >> 1) & 1) && wait_q(it + 2))) break;
         tc_fence_after();
         issue_sdp(it + 2, false);
+        mma_commit(bar_addr(sbase, B_SFULL + x));
         if constexpr (kDq) {
           if (!(ok = ctx.wait(B_DQFREE + x, (it >> 1) & 1))) break;
           tc_fence_after();
         }
         issue_sdp(it + 2, true);
-        mma_commit(bar_addr(sbase, B_SFULL + x));
+        mma_commit(bar_addr(sbase, B_DPFULL + x));
       }
     }
     __syncwarp();
@@ -464,9 +470,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_LSE);
       const float* stage_d =
           reinterpret_cast<const float*>(smem + OFF_STAGE + st * STAGE_BYTES + ST_D);
-      // QFULL: the staged LSE / D are visible here; SFULL: S^T, dP^T in TMEM.
-      // SFULL(i) is committed after dQ^T(i-2), the last reader of this
-      // block's dS^T shared buffer, so the buffer is free as well.
+      // QFULL: the staged LSE / D are visible here; SFULL: S^T in TMEM.
       if (!ctx.wait(B_QFULL + st, (it / STAGES) & 1) ||
           !ctx.wait(B_SFULL + x, (it >> 1) & 1)) {
         ok = false;
@@ -481,68 +485,86 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                              (j * BKV + BKV > N) || (window > 0 && qb + BQ > j * BKV + window);
       const int col0 = sub * 32;                      // first query column of this slice
       const uint32_t s_addr = tmem + lane_addr + 128u * x + col0;
-      uint32_t sr[32], dr[32];
-      tmem_ld32(s_addr, sr);
-      tmem_ld32(s_addr + 64, dr);
-      uint32_t pk[16], gk[16];
+      float p[32];
+      {
+        uint32_t sr[32], pk[16];
+        tmem_ld32(s_addr, sr);
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        // staged per query: -LSE*log2e and -D (two broadcast 16-byte loads)
-        float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
-        const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
-        if constexpr (kAlibi) {
-          // exponent offset -LSE log2e - slope |i - j| log2e per query column
-          if (causal) {
-            // every key the mask leaves has key <= query, so |i - j| = i - j:
-            // no absolute value, and the offsets on packed pairs
-            const uint64_t ns2 = f2pack(-slope_log2, -slope_log2);
-            const uint64_t d02 = f2pack(d0, d0);
-            const uint64_t de01 = f2add(d02, f2pack(static_cast<float>(e), static_cast<float>(e + 1)));
-            const uint64_t de23 = f2add(d02, f2pack(static_cast<float>(e + 2), static_cast<float>(e + 3)));
-            f2unpack(f2fma(ns2, de01, f2pack(l4.x, l4.y)), l4.x, l4.y);
-            f2unpack(f2fma(ns2, de23, f2pack(l4.z, l4.w)), l4.z, l4.w);
-          } else {
-            const float de = d0 + static_cast<float>(e);
-            l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
-            l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
-            l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
-            l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
+        for (int e = 0; e < 32; e += 4) {
+          // staged per query: -LSE*log2e (one broadcast 16-byte load)
+          float4 l4 = *reinterpret_cast<const float4*>(stage_lse + col0 + e);
+          if constexpr (kAlibi) {
+            // exponent offset -LSE log2e - slope |i - j| log2e per query column
+            if (causal) {
+              // every key the mask leaves has key <= query, so |i - j| = i - j:
+              // no absolute value, and the offsets on packed pairs
+              const uint64_t ns2 = f2pack(-slope_log2, -slope_log2);
+              const uint64_t d02 = f2pack(d0, d0);
+              const uint64_t de01 = f2add(d02, f2pack(static_cast<float>(e), static_cast<float>(e + 1)));
+              const uint64_t de23 = f2add(d02, f2pack(static_cast<float>(e + 2), static_cast<float>(e + 3)));
+              f2unpack(f2fma(ns2, de01, f2pack(l4.x, l4.y)), l4.x, l4.y);
+              f2unpack(f2fma(ns2, de23, f2pack(l4.z, l4.w)), l4.z, l4.w);
+            } else {
+              const float de = d0 + static_cast<float>(e);
+              l4.x = fmaf(-slope_log2, fabsf(de), l4.x);
+              l4.y = fmaf(-slope_log2, fabsf(de + 1.f), l4.y);
+              l4.z = fmaf(-slope_log2, fabsf(de + 2.f), l4.z);
+              l4.w = fmaf(-slope_log2, fabsf(de + 3.f), l4.w);
+            }
           }
+          // exponent arguments on packed fp32 pairs
+          const uint64_t sc2 = f2pack(scale_log2, scale_log2);
+          float a0, a1, a2, a3;
+          f2unpack(f2fma(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2,
+                         f2pack(l4.x, l4.y)), a0, a1);
+          f2unpack(f2fma(f2pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sc2,
+                         f2pack(l4.z, l4.w)), a2, a3);
+          float p0 = fast_exp2(a0), p1 = fast_exp2(a1), p2 = fast_exp2(a2), p3 = fast_exp2(a3);
+          if (need_mask) {
+            // qlo <= q <= qhi as one unsigned compare per query (the
+            // wrap-around of rel + t is the exact difference mod 2^32)
+            const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
+            p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
+            p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
+            p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
+            p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
+          }
+          p[e] = p0; p[e + 1] = p1; p[e + 2] = p2; p[e + 3] = p3;
+          pk[e / 2] = pack_bf16x2(p0, p1);
+          pk[e / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        // exponent arguments and dS = P (dP - D) on packed fp32 pairs
-        const uint64_t sc2 = f2pack(scale_log2, scale_log2);
-        float a0, a1, a2, a3;
-        f2unpack(f2fma(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2,
-                       f2pack(l4.x, l4.y)), a0, a1);
-        f2unpack(f2fma(f2pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sc2,
-                       f2pack(l4.z, l4.w)), a2, a3);
-        float p0 = fast_exp2(a0), p1 = fast_exp2(a1), p2 = fast_exp2(a2), p3 = fast_exp2(a3);
-        if (need_mask) {
-          // qlo <= q <= qhi as one unsigned compare per query (the
-          // wrap-around of rel + t is the exact difference mod 2^32)
-          const uint32_t rel = static_cast<uint32_t>(qb + col0 + e - qlo);
-          p0 = (row_valid && rel <= qspan) ? p0 : 0.f;
-          p1 = (row_valid && rel + 1 <= qspan) ? p1 : 0.f;
-          p2 = (row_valid && rel + 2 <= qspan) ? p2 : 0.f;
-          p3 = (row_valid && rel + 3 <= qspan) ? p3 : 0.f;
-        }
-        pk[e / 2] = pack_bf16x2(p0, p1);
-        pk[e / 2 + 1] = pack_bf16x2(p2, p3);
-        {
+        // Packed P^T over the first 16 of the 32 columns this thread has just
+        // read (no other warp reads them); dS^T takes the other 16.
+        tmem_st16(s_addr, pk);
+      }
+      // DPFULL: dP^T in TMEM.  It is committed after dQ^T(i-2), the last
+      // reader of this block's dS^T shared buffer, so the buffer is free too.
+      if (!ctx.wait(B_DPFULL + x, (it >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t gk[16];
+      {
+        uint32_t dr[32];
+        tmem_ld32(s_addr + 64, dr);
+        const uint64_t s2 = f2pack(scale, scale);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          // staged per query: -scale D (one broadcast 16-byte load);
+          // scale dS = P (scale dP - scale D) on packed fp32 pairs
+          const float4 d4 = *reinterpret_cast<const float4*>(stage_d + col0 + e);
           float g0, g1, g2, g3;
-          // scale dS = P (scale dP - scale D), the staged value being -scale D
-          const uint64_t s2 = f2pack(scale, scale);
-          f2unpack(f2mul(f2pack(p0, p1), f2fma(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                               s2, f2pack(d4.x, d4.y))), g0, g1);
-          f2unpack(f2mul(f2pack(p2, p3), f2fma(f2pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
-                                               s2, f2pack(d4.z, d4.w))), g2, g3);
+          f2unpack(f2mul(f2pack(p[e], p[e + 1]),
+                         f2fma(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), s2,
+                               f2pack(d4.x, d4.y))), g0, g1);
+          f2unpack(f2mul(f2pack(p[e + 2], p[e + 3]),
+                         f2fma(f2pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])), s2,
+                               f2pack(d4.z, d4.w))), g2, g3);
           gk[e / 2] = pack_bf16x2(g0, g1);
           gk[e / 2 + 1] = pack_bf16x2(g2, g3);
         }
       }
-      // Packed P^T and dS^T go over exactly the 32 columns this thread has
-      // just read (P^T first 16, dS^T last 16): no other warp reads them.
-      tmem_st16(s_addr, pk);
       tmem_st16(s_addr + 16, gk);
       // dS^T row into this block's shared buffer (MN-major operand of dQ^T).
       if constexpr (kDq) {
@@ -660,8 +682,9 @@ constexpr uint32_t DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
 constexpr int DQB_QFULL = 0;
 constexpr int DQB_FULL = 1;                          // + stage
 constexpr int DQB_EMPTY = DQB_FULL + DQ_STAGES;      // + stage
-constexpr int DQB_SFULL = DQB_EMPTY + DQ_STAGES;     // + buffer
-constexpr int DQB_PFULL = DQB_SFULL + 2;             // + buffer (8 warps)
+constexpr int DQB_SFULL = DQB_EMPTY + DQ_STAGES;     // + buffer: S(t) in TMEM
+constexpr int DQB_DPFULL = DQB_SFULL + 2;            // + buffer: dP(t) in TMEM
+constexpr int DQB_PFULL = DQB_DPFULL + 2;            // + buffer (8 warps)
 constexpr int DQB_DSREAD = DQB_PFULL + 2;            // + buffer: dQ(t) has read dS(t)
 constexpr int DQB_DONE = DQB_DSREAD + 2;
 constexpr int DQ_NBAR = DQB_DONE + 1;
@@ -711,6 +734,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(DQB_SFULL + x), 1);
+      mbar_init(bar(DQB_DPFULL + x), 1);
       mbar_init(bar(DQB_PFULL + x), 8);
       mbar_init(bar(DQB_DSREAD + x), 1);
     }
@@ -793,7 +817,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (lane == 0) {
       auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
       auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
-      // S(t) into buffer t & 1 and dP(t) beside it: reductions over d.
+      // S(t) into buffer t & 1 and dP(t) beside it: reductions over d, each
+      // committed to its own barrier so that the exponentials start while
+      // dP(t) is still on its way.
       auto issue_sdp = [&](int t) {
         const uint32_t buf = tmem + 128u * (t & 1);
         const uint64_t qd = sdesc_sw128(sbase + DQ_OFF_Q, 16, 1024);
@@ -811,7 +837,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           b2[kk] = vd + ob;
         }
         mma_ss_batch8(buf, a, b, IDESC_DQ_S, 0u);
+        mma_commit(bar(DQB_SFULL + (t & 1)));
         mma_ss_batch8(buf + 64, a2, b2, IDESC_DQ_S, 0u);
+        mma_commit(bar(DQB_DPFULL + (t & 1)));
       };
       bool ok = wait(DQB_QFULL, 0);
       for (int t = 0; t < nt && ok; ++t) {
@@ -820,7 +848,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (!(ok = full(t))) break;
         tc_fence_after();
         issue_sdp(t);
-        mma_commit(bar(DQB_SFULL + (t & 1)));
       }
     }
     __syncwarp();
@@ -849,30 +876,45 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       }
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_addr + 128u * x + 32 * sub;
-      uint32_t sr[32], dr[32];
-      tmem_ld32(s_addr, sr);
-      tmem_ld32(s_addr + 64, dr);
       const int j0 = (t_lo + t) * DQ_BK + 32 * sub;               // first key of this half
       const bool need_mask = !row_valid || j0 < lo || j0 + 31 > hi;
       const float d0 = static_cast<float>(q - j0);
-      uint32_t gk[16];
+      float p[32];
+      {
+        uint32_t sr[32];
+        tmem_ld32(s_addr, sr);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float b0 = nlse, b1 = nlse;
-        if constexpr (kAlibi) {
-          b0 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e)), nlse);
-          b1 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e + 1)), nlse);
+        for (int e = 0; e < 32; e += 2) {
+          float b0 = nlse, b1 = nlse;
+          if constexpr (kAlibi) {
+            b0 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e)), nlse);
+            b1 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e + 1)), nlse);
+          }
+          float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, b0));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, b1));
+          if (need_mask) {
+            const bool v0 = row_valid && j0 + e >= lo && j0 + e <= hi;
+            const bool v1 = row_valid && j0 + e + 1 >= lo && j0 + e + 1 <= hi;
+            p0 = v0 ? p0 : 0.f;
+            p1 = v1 ? p1 : 0.f;
+          }
+          p[e] = p0;
+          p[e + 1] = p1;
         }
-        float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, b0));
-        float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, b1));
-        if (need_mask) {
-          const bool v0 = row_valid && j0 + e >= lo && j0 + e <= hi;
-          const bool v1 = row_valid && j0 + e + 1 >= lo && j0 + e + 1 <= hi;
-          p0 = v0 ? p0 : 0.f;
-          p1 = v1 ? p1 : 0.f;
-        }
-        gk[e / 2] = pack_bf16x2(p0 * fmaf(__uint_as_float(dr[e]), scale, nd),
-                                p1 * fmaf(__uint_as_float(dr[e + 1]), scale, nd));
+      }
+      if (!wait(DQB_DPFULL + x, (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t gk[16];
+      {
+        uint32_t dr[32];
+        tmem_ld32(s_addr + 64, dr);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          gk[e / 2] = pack_bf16x2(p[e] * fmaf(__uint_as_float(dr[e]), scale, nd),
+                                  p[e + 1] * fmaf(__uint_as_float(dr[e + 1]), scale, nd));
       }
       // packed dS over the first 16 of the 32 columns this thread just read
       tmem_st16(s_addr, gk);
