@@ -152,30 +152,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, both operands described by shared-memory
-// matrix descriptors; kind::f16 (bf16 inputs, fp32 accumulator).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T: the A operand (M rows on TMEM lanes, K
-// along columns, two 16-bit elements per 32-bit column) is read from tensor
-// memory; B is described by a shared-memory descriptor.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
+// tcgen05.mma kind::f16: bf16 inputs, fp32 accumulator in tensor memory.
+// Shared-memory operands are given by matrix descriptors; a tensor-memory A
+// operand (the TS form) has its M rows on TMEM lanes and K along columns, two
+// 16-bit elements per 32-bit column.
 
 // 8 consecutive k-steps into one accumulator from a single asm statement:
 // D (+)= A_k B_k^T with both operands in shared memory.
