@@ -11,8 +11,9 @@ that for the backward, summed over every rank.
 
 The same line carries:
   roofline      the dominant kernel (backward dK/dV/dQ) against the measured
-                sustained bf16 tensor peak, timed with events recorded by the
-                library immediately around that kernel;
+                burst bf16 tensor peak (the timed loop is short and runs at
+                the full SM clock), timed with events recorded by the library
+                immediately around that kernel;
   e2e           the same metric through the public API with the step's inputs
                 copied from pinned host memory and dQ, dK, dV copied back;
   targets       the forward kernel alone on "bf16 causal forward B1 H32 N8192"
@@ -352,12 +353,18 @@ def run_ours(args, dist: Dist):
     del pin_in, pin_out, dev_in, dev_o, dev_g
 
     # --- roofline of the dominant kernel (the backward dK/dV/dQ kernel)
+    # The timed loop is well under a second at the full SM clock, so the
+    # denominator is the burst peak (a GEMM timed alone); the sustained peak,
+    # taken over seconds under the power cap at a lower clock, is kept as a
+    # labelled secondary figure.
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     ach = bwd_fl / (bwd_ms * 1e-3) / 1e12
     roofline = {"kernel": "bwd_main_kernel (dK, dV, dQ)", "bound": "tensor",
-                "achieved": round(ach, 1), "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": round(ach / peak_sus, 4),
-                "peak_kind": f"bf16 dense, sustained ({peak_src})",
+                "achieved": round(ach, 1), "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": round(ach / peak_burst, 4),
+                "peak_kind": f"bf16 dense, burst ({peak_src})",
+                "frac_of_sustained": round(ach / peak_sus, 4), "sustained_peak": peak_sus,
                 "flops_per_launch": bwd_fl, "ms_per_launch": round(bwd_ms, 4),
                 "traffic": recorded_traffic("bwd_bf16.cu")}
     fwd_ach = fwd_fl / (fwd_ms * 1e-3) / 1e12
@@ -468,6 +475,7 @@ def measure_targets(args, dev, peaks, peak_src):
             best = rec
     out["decode_B64_H32_L32768"] = dict(best, peak=hbm, unit="GB/s",
                                         peak_kind=f"HBM copy ({peak_src})",
+                                        timed="whole call: split kernel + combine kernel",
                                         bytes_per_launch=acc.decode_kv_bytes(w.B, w.H, w.N, w.d))
     del q, kc, vc, o
 
@@ -568,6 +576,7 @@ def measure_targets(args, dev, peaks, peak_src):
             best = rec
     out["decode_gqa_B64_Hq32_Hkv8_L32768"] = dict(best, peak=hbm, unit="GB/s",
                                                   peak_kind=f"HBM copy ({peak_src})",
+                                                  timed="whole call: split kernel + combine kernel",
                                                   bytes_per_launch=kv_bytes)
     return out
 

@@ -526,11 +526,13 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, void* o
       static_cast<const __nv_bfloat16*>(vc), part_o, part_lse, L, num_splits, chunk,
       scale * 1.4426950408889634f, alibi, H);
   cudaError_t e = cudaGetLastError();
-  if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<dim3(BH), dim3(HD), 0, stream>>>(
       part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse_out, num_splits);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  // the timed span is the whole call: the split pass and its merge
+  if (ev.after) cudaEventRecord(ev.after, stream);
+  return e;
 }
 
 cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q,
@@ -557,11 +559,12 @@ cudaError_t launch_decode_gqa(const CUtensorMap& tmK, const CUtensorMap& tmV, co
                                       part_lse, L, num_splits, chunk, group, nslice,
                                       scale * 1.4426950408889634f, alibi, Hq);
   cudaError_t e = cudaGetLastError();
-  if (ev.after) cudaEventRecord(ev.after, stream);
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<dim3(B * Hq), dim3(HD), 0, stream>>>(
       part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse_out, num_splits);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (ev.after) cudaEventRecord(ev.after, stream);
+  return e;
 }
 
 // ---------------------------------------------------------------------------

@@ -15,6 +15,11 @@ Workloads (inputs larger than the 129 MB L2, a few GB on the device at most):
           GQA training workload)
   dec_gqa bf16 GQA split-KV decode B4 Hq32 Hkv8 Lkv32768 d128, 8 splits (1/16
           of the GQA decode workload's sequences)
+  fwd_fp8 fp8 (E4M3) causal forward B1 H32 N8192 d128 (the fp8 workload
+          itself; the call runs the V transposition, then the forward)
+  fwd_fp32 fp32 forward B1 H1 N256 d64 (the tiny fp32 workload itself)
+  bwd_det bf16 causal deterministic backward B2 H32 N4096 d128 (dK/dV
+          kernel without dQ, then the query-stationary dQ kernel)
 One warm-up launch precedes the K profiled ones.  Prints the mean device
 time per launch measured with CUDA events (not a bench value under ncu).
 """
@@ -38,7 +43,7 @@ def main():
 
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["fwd", "fwd_nc", "bwd", "decode", "fwd_win", "bwd_gqa",
-                                     "dec_gqa"])
+                                     "dec_gqa", "fwd_fp8", "fwd_fp32", "bwd_det"])
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
@@ -70,6 +75,46 @@ def main():
                                            lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
                                            dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, 1,
                                            ws.data_ptr(), nbytes, sh))
+    elif a.case == "bwd_det":
+        B, H, N = 2, 32, 4096
+        q, k, v, do = inputs.attention_inputs(B, H, N, d, torch.bfloat16, 3, dev, with_do=True)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        _lib.check(_lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, scale, 1, sh))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        nbytes = _lib.fa_workspace_size(_lib.FA_OP_BACKWARD, B, H, N, d, 0)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def call():
+            _lib.check(_lib.fa_backward_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H,
+                                            N, d, scale, 1, 0, None, 1, ws.data_ptr(), nbytes,
+                                            sh))
+    elif a.case == "fwd_fp8":
+        B, H, N = 1, 32, 8192
+        q8, k8, v8 = inputs.fp8_inputs(B, H, H, N, d, 8, dev)
+        o = torch.empty((B, H, N, d), device=dev, dtype=torch.bfloat16)
+        lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        nbytes = _lib.fa_workspace_size(_lib.FA_OP_FORWARD_FP8, B, H, N, d, 0)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ds = 1.0 / inputs.FP8_AMP
+
+        def call():
+            _lib.check(_lib.fa_forward_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(),
+                                           o.data_ptr(), lse.data_ptr(), B, H, H, N, d, scale,
+                                           ds, ds, ds, 1, 0, None, ws.data_ptr(), nbytes, sh))
+    elif a.case == "fwd_fp32":
+        B, H, N, d32 = 1, 1, 256, 64
+        q, k, v = inputs.attention_inputs(B, H, N, d32, torch.float32, 0, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+
+        def call():
+            _lib.check(_lib.fa_forward_fp32(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            o.data_ptr(), lse.data_ptr(), B, H, N, d32,
+                                            1 / math.sqrt(d32), 0, sh))
     elif a.case == "fwd_win":
         B, H, N, W = 1, 32, 8192, 1024
         q, k, v = inputs.attention_inputs(B, H, N, d, torch.bfloat16, 6, dev)

@@ -347,8 +347,9 @@ int fa_selftest_timeout(unsigned limit_ms, cudaStream_t stream);
  * fa_set_timing_events -- measurement hook.  While set (both non-NULL), every
  * later call made on this host thread records `before` on its stream just
  * before launching its main kernel (the fused forward kernel, the backward
- * dK/dV/dQ kernel, or the split-KV decode kernel) and `after` just after it,
- * so cudaEventElapsedTime(before, after) is that kernel's device time.  The
+ * dK/dV/dQ kernel) and `after` just after it, so cudaEventElapsedTime(before,
+ * after) is that kernel's device time.  For the decode calls the span covers
+ * both kernels, the split pass and the combine that merges its parts.  The
  * events are created and owned by the caller.  Pass NULL, NULL to stop.
  * Returns FA_OK, or FA_ERR_INVALID_ARG if exactly one event is NULL.
  */

@@ -13,6 +13,6 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_forward_rows,
     online_softmax_stats,
-    tiled_attention_row,
+    tile_merged_attention_row,
 )
 from .fp8 import attention_forward_fp8, decode_e4m3  # noqa: F401

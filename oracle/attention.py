@@ -25,11 +25,12 @@ function cites the passage it follows):
   KV cache, no mask ("FlashAttention ontleed", "Interactie met de
   KV-cache"; Lensa ML FAQ on decoding).  It does NOT split the cache:
   split-invariance is what the GPU path has to show.
-* ``online_softmax_stats`` and ``tiled_attention_row`` -- the pages'
-  running-max / running-sum recurrence, in the pages' order, used only to
-  pin the definition against the pages' worked example and exactness claim
-  (Lensa ML "FlashAttention", step 4 "Online Softmax" and step 6;
-  "FlashAttention ontleed", "Algoritmische kern in pseudocode").
+* ``online_softmax_stats`` -- the running-max / running-sum update rule of
+  Lensa ML "FlashAttention", step 4 "Online Softmax", used only to pin the
+  definition against that page's worked example.
+* ``tile_merged_attention_row`` -- one row computed as independent tile
+  partials (o_t, lse_t) merged by their log-sum-exp weights, used only to
+  pin the exactness claim of Lensa ML "FlashAttention", step 6.
 
 Readings taken where the pages are silent:
 * causal masking means key j is hidden from query i when j > i (square,
@@ -57,7 +58,7 @@ __all__ = [
     "attention_backward",
     "attention_decode",
     "online_softmax_stats",
-    "tiled_attention_row",
+    "tile_merged_attention_row",
 ]
 
 
@@ -203,26 +204,36 @@ def online_softmax_stats(x, chunk: int):
     return trace
 
 
-def tiled_attention_row(q, k, v, scale: float, tile: int):
-    """One query row by the tiled loop of "FlashAttention ontleed",
-    section "Algoritmische kern in pseudocode": per K/V tile, the local
-    scores, the new running maximum, the rescaled exponentials, the output
-    rescaled by e^(m_old - m_new) and accumulated, and after the last tile a
-    single division by l.  Used only to pin the exactness claim of Lensa ML
+def tile_merged_attention_row(q, k, v, scale: float, tile: int):
+    """One query row (no mask) computed tile by tile, then merged.
+
+    Every tile of at most ``tile`` keys is treated as a small attention
+    problem of its own: its scores, its own maximum and sum, its normalised
+    output o_t and its log-sum-exp lse_t.  The row over all keys then
+    follows from the partials alone: with L = ln sum_t e^(lse_t), a key of
+    tile t carries weight e^(lse_t - L) times its weight inside the tile, so
+    O = sum_t e^(lse_t - L) o_t and LSE = L.  This is the rescaling behind
+    the running maximum and sum of Lensa ML "FlashAttention", step 4,
+    applied across tiles; it is used only to pin the exactness claim of
     step 6 (tiled equals standard up to rounding).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    m, l = -math.inf, 0.0
-    o = np.zeros(v.shape[-1], dtype=np.float64)
+    partials = []
     for start in range(0, k.shape[0], tile):
-        s = (k[start:start + tile] @ q) * scale
-        m_new = max(m, float(s.max()))
-        p = np.exp(s - m_new)
-        corr = math.exp(m - m_new)
-        l = corr * l + float(p.sum())
-        o = corr * o + p @ v[start:start + tile]
-        m = m_new
-    return o / l, m + math.log(l)
+        kt, vt = k[start:start + tile], v[start:start + tile]
+        s_t = (kt @ q) * scale
+        m_t = float(s_t.max())
+        e_t = np.exp(s_t - m_t)
+        l_t = float(e_t.sum())
+        partials.append(((e_t @ vt) / l_t, m_t + math.log(l_t)))
+    lses = [lse_t for _, lse_t in partials]
+    top = max(lses)
+    total = top + math.log(math.fsum(math.exp(x - top) for x in lses))
+    o = np.zeros(v.shape[-1], dtype=np.float64)
+    for o_t, lse_t in partials:
+        w = math.exp(lse_t - total)
+        o = o + w * o_t
+    return o, total
 
 
 # --------------------------------------------------------------------------

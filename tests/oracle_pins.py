@@ -125,7 +125,7 @@ def pin_exactness(orc):
         scale = 1 / math.sqrt(d)
         o_std, lse_std = orc.attention_forward(q[None, None], k[None, None], v[None, None],
                                                scale, False)
-        o_t, lse_t = orc.tiled_attention_row(q[0], k, v, scale, int(g["keys_per_tile"]))
+        o_t, lse_t = orc.tile_merged_attention_row(q[0], k, v, scale, int(g["keys_per_tile"]))
         worst = max(worst, float(np.abs(o_std[0, 0, 0] - o_t).max()),
                     abs(float(lse_std[0, 0, 0]) - lse_t))
     assert worst <= 5 * g["max_abs_diff_printed"] + 1e-16, worst

@@ -33,22 +33,3 @@ def test_decode_default_entry_point():
     assert_close_bf16(o, None, o_ref, None)
 
 
-def test_decode_b64_h32_l32768_sampled():
-    w = inputs.DECODE_L32K
-    q, kc, vc = inputs.workload_inputs(w, "cuda")
-    scale = 1 / math.sqrt(w.d)
-    outs = {s: api.decode(q, kc, vc, num_splits=s, scale=scale, with_lse=True)
-            for s in (1, 4, 16)}
-    rng = np.random.default_rng(4)
-    pairs = [(0, 0), (w.B - 1, w.H - 1)] + [tuple(x) for x in
-                                            zip(rng.integers(0, w.B, 6), rng.integers(0, w.H, 6))]
-    for b, h in pairs:
-        o_ref, lse_ref = orc.attention_decode(np64(q[b, h]), np64(kc[b, h]), np64(vc[b, h]),
-                                              scale)
-        for s, (o, lse) in outs.items():
-            assert_close_bf16(o[b, h], lse[b, h], o_ref, lse_ref, f"({b},{h}) splits={s}")
-    # split invariance over every (b, h): the parts recombine to the same answer
-    o1 = outs[1][0].float()
-    for s in (4, 16):
-        assert (outs[s][0].float() - o1).abs().max().item() <= 2 * O_MAX
-        assert (outs[s][1] - outs[1][1]).abs().max().item() <= LSE_MAX

@@ -45,28 +45,6 @@ def test_bf16_forward_b4_h16_n2048(causal):
     assert_close_bf16(o, lse, o_ref, lse_ref, f"causal={causal}")
 
 
-def test_bf16_long_causal_n8192_sampled():
-    w = inputs.LONG_CAUSAL
-    q, k, v = inputs.workload_inputs(w, "cuda")
-    scale = 1 / math.sqrt(w.d)
-    o, lse = api.forward(q, k, v, causal=True, scale=scale)
-    rng = np.random.default_rng(2)
-    rows = np.unique(np.concatenate([np.arange(64), np.arange(w.N - 64, w.N),
-                                     rng.choice(w.N, 256, replace=False)]))
-    for h in (0, 13, w.uniform_head):
-        kh, vh = np64(k[0, h]), np64(v[0, h])
-        o_ref, lse_ref = orc.attention_forward_rows(np64(q[0, h, rows]), kh, vh, rows, scale,
-                                                    True)
-        assert_close_bf16(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, f"head {h}")
-    # the uniform head: every visible key has the same weight
-    h = w.uniform_head
-    vh = np64(v[0, h])
-    mean_prefix = np.cumsum(vh, axis=0) / np.arange(1, w.N + 1)[:, None]
-    assert np.abs(np64(o[0, h]) - mean_prefix).max() <= O_MAX
-
-
-
-
 def test_bf16_forward_split_tail_items_ragged_gqa():
     """Non-causal, 160 (Q pair, head) items on 152 SMs: the last 8 items run
     as 16 one-tile blocks.  They are the last Q pair (tiles 18 and 19, the

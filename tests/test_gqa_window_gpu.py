@@ -104,61 +104,7 @@ def test_decode_gqa(B, Hq, Hkv, L, splits):
     assert guards_intact(bo)
 
 
-# ------------------------------------------------------- full-size, sampled
-def test_gqa_train_b8_hq32_hkv8_n4096_sampled():
-    w = inputs.GQA_TRAIN_N4096
-    q, k, v, do = inputs.workload_inputs(w, "cuda")
-    o, lse = api.forward(q, k, v, causal=True, scale=SCALE)
-    dq, dk, dv = api.backward(q, k, v, o, lse, do, causal=True, scale=SCALE)
-    g = w.H // w.kv_heads
-    for b, t in ((0, 0), (7, 7), (3, 5)):
-        hs = slice(t * g, (t + 1) * g)
-        args = (np64(q[b:b + 1, hs]), np64(k[b:b + 1, t:t + 1]), np64(v[b:b + 1, t:t + 1]))
-        o_ref, lse_ref = orc.attention_forward_gqa(*args, SCALE, True)
-        assert_close_bf16(o[b:b + 1, hs], lse[b:b + 1, hs], o_ref, lse_ref, f"fwd ({b},{t})")
-        refs = orc.attention_backward_gqa(*args, np64(do[b:b + 1, hs]), SCALE, True)
-        for name, got, ref in zip(("dq", "dk", "dv"),
-                                  (dq[b:b + 1, hs], dk[b:b + 1, t:t + 1], dv[b:b + 1, t:t + 1]),
-                                  refs):
-            err = np.abs(np64(got) - ref).max()
-            assert err <= G_MAX, f"{name} ({b},{t}) max err {err:.3e}"
-
-
-def test_window_n8192_sampled():
-    w = inputs.WINDOW_N8192
-    q, k, v = inputs.workload_inputs(w, "cuda")
-    o, lse = api.forward(q, k, v, causal=True, scale=SCALE, window=w.window)
-    rng = np.random.default_rng(6)
-    rows = np.unique(np.concatenate([np.arange(64), np.arange(w.window - 64, w.window + 192),
-                                     np.arange(w.N - 64, w.N),
-                                     rng.choice(w.N, 256, replace=False)]))
-    for h in (0, 19, 31):
-        o_ref, lse_ref = orc.attention_forward_rows(np64(q[0, h, rows]), np64(k[0, h]),
-                                                    np64(v[0, h]), rows, SCALE, True,
-                                                    window=w.window)
-        assert_close_bf16(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, f"head {h}")
-
-
-def test_gqa_decode_b64_hq32_hkv8_l32768_sampled():
-    w = inputs.GQA_DECODE_L32K
-    q, kc, vc = inputs.workload_inputs(w, "cuda")
-    g = w.H // w.kv_heads
-    outs = {s: api.decode(q, kc, vc, num_splits=s, scale=SCALE, with_lse=True)
-            for s in (1, 2, 4, 8)}
-    for b, h in ((0, 0), (63, 31), (17, 9), (40, 22)):
-        t = h // g
-        o_ref, lse_ref = orc.attention_decode_gqa(np64(q[b:b + 1, h:h + 1]),
-                                                  np64(kc[b:b + 1, t:t + 1]),
-                                                  np64(vc[b:b + 1, t:t + 1]), SCALE)
-        for s, (o, lse) in outs.items():
-            assert_close_bf16(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], o_ref, lse_ref,
-                              f"({b},{h}) splits={s}")
-    # split counts agree with each other everywhere
-    base = outs[1][0].float()
-    for s in (2, 4, 8):
-        assert (outs[s][0].float() - base).abs().max().item() <= O_MAX
-
-
+# ------------------------------------------------------- automatic split count
 @pytest.mark.parametrize("B,Hq,Hkv,L", [(2, 8, 2, 5000), (4, 4, 4, 3000)])
 def test_decode_automatic_splits(B, Hq, Hkv, L):
     q, kc, vc = inputs.decode_gqa_inputs(B, Hq, Hkv, L, D, torch.bfloat16, 140 + L, "cuda")

@@ -47,8 +47,9 @@ MUTANTS = {
     "alibi_next_head": ("return None if alibi_slopes is None else float(alibi_slopes[h])",
                         "return None if alibi_slopes is None else float(alibi_slopes[(h + 1) % len(alibi_slopes)])"),
     "alibi_decode_position": ("(s.shape[0] - 1 - np.arange(s.shape[0]))", "(s.shape[0] - np.arange(s.shape[0]))"),
-    "tiled_no_out_rescale": ("o = corr * o + p @ v[start:start + tile]",
-                             "o = o + p @ v[start:start + tile]"),
+    "tile_merge_weight_unnormalised": ("w = math.exp(lse_t - total)", "w = math.exp(lse_t - top)"),
+    "tile_partial_unnormalised": ("partials.append(((e_t @ vt) / l_t, m_t + math.log(l_t)))",
+                                  "partials.append((e_t @ vt, m_t + math.log(l_t)))"),
 }
 
 

@@ -3,11 +3,15 @@ query and key/value head counts, sequence lengths that hit every tile
 remainder, the causal mask, windows, ALiBi and the deterministic backward
 drawn together, with guarded outputs.  Decode draws cache lengths and split
 counts the same way.  Tolerances as elsewhere (O max 2e-2 / mean 2e-3, LSE
-1e-3, gradients 5e-2), except that the drawn scales go up to 0.2 (2.3 times
-1/sqrt(d)), where peaked rows give gradients of magnitude ~10-30: a bf16
-result is then off by up to half a unit in its last place, 2^-8 |g|, before
-any arithmetic, so each gradient element may also differ by 2^-7 |g_ref|
-(that rounding plus as much again for the bf16 P and dS operands)."""
+1e-3, gradients 5e-2 against the oracle's exact-O gradients) for every draw
+at the workloads' scale 1/sqrt(d) or below (0.05).  The draws at scale 0.2
+(2.3 times 1/sqrt(d)) have peaked rows with gradients of magnitude ~10-30: a
+bf16 result is then off by up to half a unit in its last place, 2^-8 |g|,
+before any arithmetic, so there each gradient element may also differ by
+2^-7 |g_ref| (that rounding plus as much again for the bf16 P and dS
+operands), and D = rowsum(dO * O) is formed from the O the forward stored,
+as the kernel forms it (where dP - D cancels in a nearly one-hot row, the
+rounding of O to bf16 moves D by more than the gradient tolerance)."""
 import math
 
 import numpy as np
@@ -59,11 +63,13 @@ def test_random_forward_backward(seed):
     bv, dv = guarded((B, Hkv, N, D), torch.bfloat16)
     api.backward(q, k, v, o, lse, do, causal=c["causal"], scale=c["scale"], out=(dq, dk, dv),
                  window=c["window"], alibi_slopes=slopes, deterministic=c["det"])
+    plain = c["scale"] <= 1 / math.sqrt(D) + 1e-12
     refs = orc.attention_backward_gqa(np64(q), np64(k), np64(v), np64(do), c["scale"],
-                                      c["causal"], win, sl, o=np64(o))
+                                      c["causal"], win, sl, o=None if plain else np64(o))
+    rel = 0.0 if plain else 2.0 ** -7
     for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
         err = np.abs(np64(got) - ref)
-        over = (err / (G_MAX + 2.0 ** -7 * np.abs(ref))).max()
+        over = (err / (G_MAX + rel * np.abs(ref))).max()
         assert over <= 1.0, f"{name} max err {err.max():.3e} (x{over:.2f} of the bound) {c}"
     assert guards_intact(bq) and guards_intact(bk) and guards_intact(bv)
 
