@@ -175,13 +175,25 @@ def lib_event():
     return e
 
 
-def kernel_source_hash(name: str) -> str:
-    p = os.path.join(ROOT, "exact_attention_84_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_hash(name: str, upto: str | None = None) -> str:
+    """Hash of a kernel's source: its file up to the marker `upto` (the
+    kernels of a file come before their launchers, so a change to a later
+    kernel or to host code leaves the hash alone) plus the shared device
+    header."""
+    csrc = os.path.join(ROOT, "exact_attention_84_gb300", "csrc")
+    with open(os.path.join(csrc, name), "rb") as f:
+        text = f.read()
+    if upto is not None:
+        cut = text.find(upto.encode())
+        if cut < 0:
+            return "marker-missing"
+        text = text[:cut]
+    with open(os.path.join(csrc, "fa_device.cuh"), "rb") as f:
+        text += f.read()
+    return hashlib.sha256(text).hexdigest()[:16]
 
 
-def recorded_traffic(kernel_file: str):
+def recorded_traffic(key: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel
     source is unchanged since the capture; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -189,8 +201,9 @@ def recorded_traffic(kernel_file: str):
         return None
     with open(p) as f:
         d = json.load(f)
-    rec = d.get(kernel_file)
-    if not rec or rec.get("source_sha256_16") != kernel_source_hash(kernel_file):
+    rec = d.get(key)
+    if not rec or rec.get("source_sha256_16") != kernel_source_hash(rec["file"],
+                                                                     rec.get("hash_upto")):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -366,7 +379,7 @@ def run_ours(args, dist: Dist):
                 "peak_kind": f"bf16 dense, burst ({peak_src})",
                 "frac_of_sustained": round(ach / peak_sus, 4), "sustained_peak": peak_sus,
                 "flops_per_launch": bwd_fl, "ms_per_launch": round(bwd_ms, 4),
-                "traffic": recorded_traffic("bwd_bf16.cu")}
+                "traffic": recorded_traffic("bwd_main_kernel")}
     fwd_ach = fwd_fl / (fwd_ms * 1e-3) / 1e12
     step_parts = {"forward_ms": round(fwd_ms, 4), "forward_tflops": round(fwd_ach, 1),
                   "backward_main_ms": round(bwd_ms, 4),

@@ -23,9 +23,9 @@ FP32_TOL = 1e-5
 
 
 def np64(t):
-    if isinstance(t, np.ndarray):
-        return t.astype(np.float64)
-    return t.detach().float().cpu().numpy().astype(np.float64)
+    if isinstance(t, torch.Tensor):
+        return t.detach().float().cpu().numpy().astype(np.float64)
+    return np.asarray(t, dtype=np.float64)
 
 
 def assert_close_bf16(o, lse, o_ref, lse_ref, what=""):
