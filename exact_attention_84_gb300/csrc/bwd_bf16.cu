@@ -108,6 +108,8 @@ constexpr int WARP_MMA3 = 15;
 // row, g query heads per key/value head) pass ~128 MB of L2.
 constexpr int kHeadGroupKv = 8;
 constexpr long long kHeadGroupBytes = 128ll << 20;
+// The deterministic dQ kernel's groups: key/value heads whose K and V fit here.
+constexpr long long kDqGroupBytes = 32ll << 20;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: M = 128 keys, N = 64 queries.
@@ -661,22 +663,27 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 // Deterministic dQ (the dQ half of the gradient without atomics): one thread
 // block per (query head, 128-query block i), K_j / V_j streamed in 64-key
 // tiles in increasing key order, dQ_i accumulated in TMEM and written once:
-//   S = Q_i K_j^T, dP = dO_i V_j^T            (shared-memory operands)
+//   S = Q_i K_j^T, dP = dO_i V_j^T            (Q_i, dO_i from TMEM)
 //   P = exp2(S scale log2e - LSE log2e [- ALiBi]),  dS = scale P * (dP - D)
 //   dQ_i += dS K_j                             (dS from TMEM, K_j MN-major)
-// Two TMEM buffers of [S | dP] let the softmax of tile t overlap the
-// products of tiles t-1 and t+1.  Each dQ element is summed by one thread
-// block in a fixed order, so the result is the same on every run.
+// Q_i and dO_i stay for the whole block, so they are copied into tensor
+// memory once and every product takes its A operand from there: per key
+// tile only K_j (twice) and V_j are read from shared memory.  Two TMEM
+// buffers of [S | dP] let the softmax of tile t overlap the products of
+// tiles t-1 and t+1.  Each dQ element is summed by one thread block in a
+// fixed order, so the result is the same on every run.
 constexpr int DQ_BQ = 128;                     // query rows (TMEM lanes)
 constexpr int DQ_BK = 64;                      // keys per tile
-constexpr int DQ_STAGES = 4;
+constexpr int DQ_STAGES = 6;
 constexpr uint32_t DQ_QTILE = DQ_BQ * HD * 2;  // Q_i or dO_i: 32 KiB
 constexpr uint32_t DQ_QHALF = DQ_QTILE / 2;    // 128 rows x 64 columns
 constexpr uint32_t DQ_KTILE = DQ_BK * HD * 2;  // K_j or V_j: 16 KiB
 constexpr uint32_t DQ_KHALF = DQ_KTILE / 2;    // 64 rows x 64 columns
-constexpr uint32_t DQ_OFF_Q = 0;
-constexpr uint32_t DQ_OFF_DO = DQ_QTILE;
-constexpr uint32_t DQ_OFF_RING = 2 * DQ_QTILE;
+constexpr uint32_t DQ_OFF_RING = 0;
+// Q_i and dO_i land in the space of ring stages 4 and 5; once they have been
+// copied into tensor memory, that space joins the K/V ring.
+constexpr uint32_t DQ_OFF_Q = 4 * 2 * DQ_KTILE;
+constexpr uint32_t DQ_OFF_DO = DQ_OFF_Q + DQ_QTILE;
 constexpr uint32_t DQ_STAGE = 2 * DQ_KTILE;    // K_j then V_j
 constexpr uint32_t DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
 constexpr int DQB_QFULL = 0;
@@ -687,11 +694,15 @@ constexpr int DQB_DPFULL = DQB_SFULL + 2;            // + buffer: dP(t) in TMEM
 constexpr int DQB_PFULL = DQB_DPFULL + 2;            // + buffer (8 warps)
 constexpr int DQB_DSREAD = DQB_PFULL + 2;            // + buffer: dQ(t) has read dS(t)
 constexpr int DQB_DONE = DQB_DSREAD + 2;
-constexpr int DQ_NBAR = DQB_DONE + 1;
+constexpr int DQB_QTMEM = DQB_DONE + 1;              // Q_i, dO_i copied to TMEM (8 warps)
+constexpr int DQ_NBAR = DQB_QTMEM + 1;
 constexpr uint32_t DQ_OFF_MISC = DQ_OFF_BAR + DQ_NBAR * 8;
 constexpr uint32_t DQ_SMEM = DQ_OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
+static_assert(DQ_SMEM <= 227u * 1024u, "dQ kernel shared memory exceeds the per-block limit");
 constexpr int DQ_THREADS = 352;                // 0-7 softmax, 8 producer, 9-10 MMA issuers
 constexpr uint32_t DQ_TM_DQ = 256;             // buffer x: S at 128x, dP at 128x + 64
+constexpr uint32_t DQ_TM_Q = 384;              // Q_i packed bf16: 64 columns
+constexpr uint32_t DQ_TM_DO = 448;             // dO_i packed bf16: 64 columns
 constexpr uint32_t IDESC_DQ_S = idesc_bf16(DQ_BQ, DQ_BK, false, false);
 constexpr uint32_t IDESC_DQ_ACC = idesc_bf16(DQ_BQ, HD, false, true);
 
@@ -701,7 +712,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const float* __restrict__ lse_pad, const float* __restrict__ d_pad,
               __nv_bfloat16* __restrict__ dQ, int BH, int N, int Npad, float scale, int causal,
-              int group, int window, const float* __restrict__ alibi, int heads) {
+              int group, int window, const float* __restrict__ alibi, int heads,
+              int head_group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -714,10 +726,17 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Blocks are ordered by groups of head_group query heads (whole key/value
+  // heads), so the thread blocks in flight share a few heads' K and V and
+  // re-read them from L2, not HBM; within a group, query blocks go
+  // heavy-first (the last block sees the most keys when causal).
   const int npb = (N + DQ_BQ - 1) / DQ_BQ;
-  const int qblk = causal ? npb - 1 - static_cast<int>(blockIdx.x) / BH
-                          : static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int per_group = head_group * npb;
+  const int hgrp = static_cast<int>(blockIdx.x) / per_group;
+  const int gsize = min(head_group, BH - hgrp * head_group);
+  const int rem = static_cast<int>(blockIdx.x) - hgrp * per_group;
+  const int qblk = causal ? npb - 1 - rem / gsize : rem / gsize;
+  const int bh = hgrp * head_group + rem % gsize;
   const int bkv = bh / group;
   const int q0 = qblk * DQ_BQ;
   // keys seen by some row of the block: [key_lo, key_hi)
@@ -739,6 +758,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(bar(DQB_DSREAD + x), 1);
     }
     mbar_init(bar(DQB_DONE), 1);
+    mbar_init(bar(DQB_QTMEM), 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -767,6 +787,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       for (int t = 0; t < nt; ++t) {
         const int st = t % DQ_STAGES;
         if (t >= DQ_STAGES && !wait(DQB_EMPTY + st, ((t / DQ_STAGES) - 1) & 1)) break;
+        // stages 4 and 5 hold Q_i and dO_i until they are in tensor memory
+        if (t >= 4 && t < DQ_STAGES && !wait(DQB_QTMEM, 0)) break;
         const uint32_t fb = bar(DQB_FULL + st);
         const uint32_t dst = sbase + DQ_OFF_RING + st * DQ_STAGE;
         const int key = (t_lo + t) * DQ_BK;
@@ -819,35 +841,30 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
       // S(t) into buffer t & 1 and dP(t) beside it: reductions over d, each
       // committed to its own barrier so that the exponentials start while
-      // dP(t) is still on its way.
-      auto issue_sdp = [&](int t) {
-        const uint32_t buf = tmem + 128u * (t & 1);
-        const uint64_t qd = sdesc_sw128(sbase + DQ_OFF_Q, 16, 1024);
-        const uint64_t dod = sdesc_sw128(sbase + DQ_OFF_DO, 16, 1024);
-        const uint64_t kd = sdesc_sw128(ring(t), 16, 1024);
-        const uint64_t vd = sdesc_sw128(ring(t) + DQ_KTILE, 16, 1024);
-        uint64_t a[8], b[8], a2[8], b2[8];
+      // dP(t) is still on its way.  A (Q_i or dO_i) comes from TMEM, 16
+      // elements of d = 8 packed columns per step.
+      auto issue = [&](int t, bool dp) {
+        const uint32_t buf = tmem + 128u * (t & 1) + (dp ? 64u : 0u);
+        const uint64_t bd = sdesc_sw128(ring(t) + (dp ? DQ_KTILE : 0u), 16, 1024);
+        uint32_t a[8];
+        uint64_t b[8];
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t oa = ((kk >> 2) * DQ_QHALF + (kk & 3) * 32) >> 4;
-          const uint64_t ob = ((kk >> 2) * DQ_KHALF + (kk & 3) * 32) >> 4;
-          a[kk] = qd + oa;
-          b[kk] = kd + ob;
-          a2[kk] = dod + oa;
-          b2[kk] = vd + ob;
+          a[kk] = tmem + (dp ? DQ_TM_DO : DQ_TM_Q) + 8 * kk;
+          b[kk] = bd + (((kk >> 2) * DQ_KHALF + (kk & 3) * 32) >> 4);
         }
-        mma_ss_batch8(buf, a, b, IDESC_DQ_S, 0u);
-        mma_commit(bar(DQB_SFULL + (t & 1)));
-        mma_ss_batch8(buf + 64, a2, b2, IDESC_DQ_S, 0u);
-        mma_commit(bar(DQB_DPFULL + (t & 1)));
+        mma_ts_batch8(buf, a, b, IDESC_DQ_S, 0u);
+        mma_commit(bar((dp ? DQB_DPFULL : DQB_SFULL) + (t & 1)));
       };
-      bool ok = wait(DQB_QFULL, 0);
+      bool ok = wait(DQB_QTMEM, 0);
+      tc_fence_after();
       for (int t = 0; t < nt && ok; ++t) {
         // buffer t & 1 holds dS(t - 2) until dQ(t - 2) has read it
         if (t >= 2 && !(ok = wait(DQB_DSREAD + (t & 1), ((t - 2) >> 1) & 1))) break;
         if (!(ok = full(t))) break;
         tc_fence_after();
-        issue_sdp(t);
+        issue(t, false);
+        issue(t, true);
       }
     }
     __syncwarp();
@@ -867,8 +884,33 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // keys this row sees: [lo, hi]
     const int lo = window > 0 ? q - window + 1 : 0;
     const int hi = causal ? min(q, N - 1) : N - 1;
-    bool ok = true;
-    for (int t = 0; t < nt; ++t) {
+    // Q_i (warps 0-3) or dO_i (warps 4-7), row by row, into tensor memory:
+    // column c holds elements 2c and 2c+1 of the row (the A-operand layout).
+    bool ok = wait(DQB_QFULL, 0);
+    if (ok) {
+      const uint8_t* tile = smem + (sub == 0 ? DQ_OFF_Q : DQ_OFF_DO);
+      const uint32_t col = sub == 0 ? DQ_TM_Q : DQ_TM_DO;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + h * DQ_QHALF +
+                                                          sw128_offset(row, c));
+          r[4 * c] = v.x;
+          r[4 * c + 1] = v.y;
+          r[4 * c + 2] = v.z;
+          r[4 * c + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_addr + col + 32 * h, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      fence_proxy_async_smem();   // the tiles' space is refilled by TMA next
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(DQB_QTMEM));
+    }
+    for (int t = 0; t < nt && ok; ++t) {
       const int x = t & 1;
       if (!wait(DQB_SFULL + x, (t >> 1) & 1)) {
         ok = false;
@@ -883,6 +925,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       {
         uint32_t sr[32];
         tmem_ld32(s_addr, sr);
+        const uint64_t sc2 = f2pack(scale_log2, scale_log2);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float b0 = nlse, b1 = nlse;
@@ -890,8 +933,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             b0 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e)), nlse);
             b1 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e + 1)), nlse);
           }
-          float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), scale_log2, b0));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), scale_log2, b1));
+          // exponent arguments on a packed fp32 pair
+          float a0, a1;
+          f2unpack(f2fma(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2,
+                         f2pack(b0, b1)), a0, a1);
+          float p0 = fast_exp2(a0);
+          float p1 = fast_exp2(a1);
           if (need_mask) {
             const bool v0 = row_valid && j0 + e >= lo && j0 + e <= hi;
             const bool v1 = row_valid && j0 + e + 1 >= lo && j0 + e + 1 <= hi;
@@ -911,10 +958,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       {
         uint32_t dr[32];
         tmem_ld32(s_addr + 64, dr);
+        const uint64_t s2 = f2pack(scale, scale), nd2 = f2pack(nd, nd);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          gk[e / 2] = pack_bf16x2(p[e] * fmaf(__uint_as_float(dr[e]), scale, nd),
-                                  p[e + 1] * fmaf(__uint_as_float(dr[e + 1]), scale, nd));
+        for (int e = 0; e < 32; e += 2) {
+          // scale dS = P (scale dP - scale D) on a packed fp32 pair
+          float g0, g1;
+          f2unpack(f2mul(f2pack(p[e], p[e + 1]),
+                         f2fma(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), s2,
+                               nd2)), g0, g1);
+          gk[e / 2] = pack_bf16x2(g0, g1);
+        }
       }
       // packed dS over the first 16 of the 32 columns this thread just read
       tmem_st16(s_addr, gk);
@@ -1027,10 +1080,16 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   if (deterministic) {
     // dQ by query blocks, in a fixed key order, written once (no atomics)
     const int npb = (N + DQ_BQ - 1) / DQ_BQ;
+    // whole key/value heads per group, their K and V (512 B per key row)
+    // within ~32 MB of L2
+    long long kv_fit = kDqGroupBytes / (static_cast<long long>(N) * 512);
+    kv_fit = kv_fit < 1 ? 1 : (kv_fit > kHeadGroupKv ? kHeadGroupKv : kv_fit);
+    const int dq_group = static_cast<int>(kv_fit) * g;   // query heads per group
     auto dqk = alibi ? bwd_dq_kernel<true> : bwd_dq_kernel<false>;
     dqk<<<dim3(npb * BH), dim3(DQ_THREADS), DQ_SMEM, stream>>>(
         dq_maps->q, dq_maps->k, dq_maps->v, dq_maps->dO, lse_pad, d_pad,
-        static_cast<__nv_bfloat16*>(dq), BH, N, Npad, scale, causal, g, window, alibi, H);
+        static_cast<__nv_bfloat16*>(dq), BH, N, Npad, scale, causal, g, window, alibi, H,
+        dq_group);
     return cudaGetLastError();
   }
   const size_t n8 = rows * HD / 8;

@@ -20,8 +20,8 @@ namespace {
 
 __device__ int g_status_fwd_fp32;   // no waits here; kept for a uniform status API
 
-constexpr int kRowsPerBlock = 16;   // 4 warps x 4 query rows
-constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerBlock = 8;    // 4 warps x 2 query rows
+constexpr int kRowsPerWarp = 2;
 constexpr int kKeysPerTile = 32;    // one key per lane
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -84,11 +84,15 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int r = warp * kRowsPerWarp + rr;
       const int qi = q0 + r;
-      // 1. local score of key (k0 + lane) for this row
-      float s = 0.f;
+      // 1. local score of key (k0 + lane) for this row (four independent
+      // partial sums, so the dot product is not one long dependent chain)
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-      for (int c = 0; c < D; ++c) s = fmaf(sQ[r][c], sK[lane][c], s);
-      s *= scale;
+      for (int c = 0; c < D; c += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) s4[u] = fmaf(sQ[r][c + u], sK[lane][c + u], s4[u]);
+      }
+      float s = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * scale;
       const int kj = k0 + lane;
       const bool valid = (kj < N) && (!causal || kj <= qi);
       s = valid ? s : -INFINITY;

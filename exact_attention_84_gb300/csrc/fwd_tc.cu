@@ -92,6 +92,7 @@ struct FwdLayout {
   static constexpr int NBAR = B_OSTG + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
+  static_assert(SMEM_BYTES <= 227u * 1024u, "forward shared memory exceeds the per-block limit");
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -104,6 +105,8 @@ constexpr int WARP_MMA = 9;
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// Block order: the K and V of the heads whose blocks run together.
+constexpr long long kFwdGroupBytes = 32ll << 20;
 
 // ---- bf16: 128 x 128 tiles as two 64-column (128-byte) swizzled boxes.
 struct Bf16 : FwdLayout<BM * HD * 2, 4> {
@@ -236,7 +239,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
                                          float* __restrict__ LSE, int BH, int N,
                                          float scale_log2, float out_scale, int causal,
                                          int group, int window, const float* __restrict__ alibi,
-                                         int heads, int nsplit) {
+                                         int heads, int nsplit, int head_group) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -259,8 +262,16 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
   const int bid = static_cast<int>(blockIdx.x);
   const int item = bid < nfull ? bid : nfull + (bid - nfull) / 2;
   const bool has_b = bid < nfull;                 // this block runs Q block B too
-  const int pair = causal ? (npair - 1 - item / BH) : (item / BH);
-  const int bh = item % BH;
+  // Items go in groups of head_group query heads (whole key/value heads), so
+  // the blocks in flight share a few heads' K and V and re-read them from L2
+  // rather than HBM; within a group Q pairs go heavy-first (causal), heads
+  // fastest.
+  const int per_group = head_group * npair;
+  const int hgrp = item / per_group;
+  const int gsize = min(head_group, BH - hgrp * head_group);
+  const int rem = item - hgrp * per_group;
+  const int pair = causal ? (npair - 1 - rem / gsize) : (rem / gsize);
+  const int bh = hgrp * head_group + rem % gsize;
   // Q tile of block A: the pair's first, or for a split item its own tile
   const int qt_a = 2 * pair + (has_b ? 0 : (bid - nfull) & 1);
   const int bkv = bh / group;                   // key/value head of this query head
@@ -609,9 +620,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                 __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int BH, int N,
                 float scale_log2, int causal, int group, int window,
-                const float* __restrict__ alibi, int heads, int nsplit) {
+                const float* __restrict__ alibi, int heads, int nsplit, int head_group) {
   fwd_body<Bf16, kWindow, kAlibi>(&tmQ, &tmK, &tmV, &tmO, O, LSE, BH, N, scale_log2, 1.f,
-                                  causal, group, window, alibi, heads, nsplit);
+                                  causal, group, window, alibi, heads, nsplit, head_group);
 }
 
 // Q, K e4m3 [BH, N, 128]; tmV maps the transposed copy V^T [BH, 128, keys].
@@ -620,9 +631,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmVt, __nv_bfloat16* __restrict__ O,
                float* __restrict__ LSE, int BH, int N, float scale_log2, float v_descale,
-               int causal, int group, int window, const float* __restrict__ alibi, int heads) {
+               int causal, int group, int window, const float* __restrict__ alibi, int heads,
+               int head_group) {
   fwd_body<Fp8, kWindow, kAlibi>(&tmQ, &tmK, &tmVt, nullptr, O, LSE, BH, N, scale_log2,
-                                 v_descale, causal, group, window, alibi, heads, 0);
+                                 v_descale, causal, group, window, alibi, heads, 0, head_group);
 }
 
 // V [rows, 128] e4m3 -> V^T [128, ld] per head, 64 keys x 128 columns per
@@ -681,6 +693,16 @@ cudaError_t set_smem(K kernel, uint32_t bytes) {
                               static_cast<int>(bytes));
 }
 
+// Query heads per group of the block order: whole key/value heads (g query
+// heads each) whose K and V (2 N 128 elem_bytes bytes per key/value head)
+// stay within kFwdGroupBytes of L2.
+int forward_head_group(int BH, int g, int N, int elem_bytes) {
+  long long kv = kFwdGroupBytes / (2ll * N * 128 * elem_bytes);
+  kv = kv < 1 ? 1 : kv;
+  const long long heads = kv * g;
+  return static_cast<int>(heads < BH ? heads : BH);
+}
+
 }  // namespace
 
 cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B, int H,
@@ -715,10 +737,11 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
       if (items > sms && r > 0 && 2 * r <= sms) nsplit = static_cast<int>(r);
     }
   }
+  const int head_group = forward_head_group(BH, H / Hkv, N, 2);
   if (ev.before) cudaEventRecord(ev.before, stream);
   kernel<<<dim3(npair * BH + nsplit), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.o, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2,
-      causal, H / Hkv, window, alibi, H, nsplit);
+      causal, H / Hkv, window, alibi, H, nsplit, head_group);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;
@@ -756,10 +779,11 @@ cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, 
   const float scale_log2 = scale * q_descale * k_descale * 1.4426950408889634f;
   auto kernel = alibi ? (window > 0 ? fwd_fp8_kernel<true, true> : fwd_fp8_kernel<false, true>)
                       : (window > 0 ? fwd_fp8_kernel<true, false> : fwd_fp8_kernel<false, false>);
+  const int head_group = forward_head_group(BH, H / Hkv, N, 1);
   if (ev.before) cudaEventRecord(ev.before, stream);
   kernel<<<dim3(npair * BH), dim3(NTHREADS), Fp8::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, v_descale,
-      causal, H / Hkv, window, alibi, H);
+      causal, H / Hkv, window, alibi, H, head_group);
   cudaError_t e = cudaGetLastError();
   if (ev.after) cudaEventRecord(ev.after, stream);
   return e;
