@@ -88,10 +88,14 @@ struct FwdLayout {
   static constexpr int B_SFULL = B_EMPTY + SLOTS;   // + block (A = 0, B = 1)
   static constexpr int B_PFULL = B_SFULL + 2;       // + block
   static constexpr int B_ODONE = B_PFULL + 2;       // + block
-  static constexpr int B_OSTG = B_ODONE + 2;        // + block: O staged (4 warps arrive)
-  static constexpr int NBAR = B_OSTG + 2;
+  static constexpr int B_OSTG = B_ODONE + 2;        // + block: O staged (softmax warps arrive)
+  static constexpr int B_XCHG = B_OSTG + 2;         // + 4 block + quadrant: row parts met
+  static constexpr int NBAR = B_XCHG + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
+  // partial row maxima / sums of the two parts of each row (two softmax
+  // warps per row): [parity][block][part][row] floats
+  static constexpr uint32_t OFF_XCHG = (OFF_MISC + 16 + 15) & ~15u;
+  static constexpr uint32_t SMEM_BYTES = OFF_XCHG + 2 * 2 * 2 * 128 * 4 + 1024;   // + alignment slack
   static_assert(SMEM_BYTES <= 227u * 1024u, "forward shared memory exceeds the per-block limit");
 };
 
@@ -99,9 +103,15 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;          // + 128 * block
 constexpr uint32_t TM_O = 256;        // + 128 * block
 
-constexpr int NTHREADS = 320;
-constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
+// Softmax warps per row: two for the ALiBi variants, whose heavier per-score
+// work makes the softmax the longer side of the ping-pong (measured 7%
+// faster), one otherwise (two measured 5% slower there: the MMA-issuing warp
+// then shares its sub-partition with four softmax warps instead of two).
+// Warps: 8 KH softmax, then the TMA producer, then the MMA issuer.
+template <bool kAlibi>
+__host__ __device__ constexpr int row_warps() { return kAlibi ? 2 : 1; }
+template <bool kAlibi>
+__host__ __device__ constexpr int fwd_threads() { return 32 * (8 * row_warps<kAlibi>() + 2); }
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -215,6 +225,19 @@ struct Fp8 : FwdLayout<BM * HD, 8> {
   }
 };
 
+// Each thread reads 64 consecutive 32-bit columns of its own TMEM lane in
+// one instruction (used when two softmax warps share a row); the load and
+// its wait are one asm statement.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
 template <class T>
 struct Ctx {
   uint32_t sbase;
@@ -251,6 +274,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int KH = row_warps<kAlibi>();       // softmax warps per row
+  constexpr int HC = BN / KH;                   // key columns of a tile per softmax warp
+  constexpr int WARP_TMA = 8 * KH;
+  constexpr int WARP_MMA = 8 * KH + 1;
 
   const int npair = (N + 2 * BM - 1) / (2 * BM);
   const int nkv = (N + BN - 1) / BN;
@@ -289,10 +316,11 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(ctx.bar(T::B_SFULL + b), 1);
-      mbar_init(ctx.bar(T::B_PFULL + b), 4);
+      mbar_init(ctx.bar(T::B_PFULL + b), 4 * KH);
       mbar_init(ctx.bar(T::B_ODONE + b), 1);
-      mbar_init(ctx.bar(T::B_OSTG + b), 4);
+      mbar_init(ctx.bar(T::B_OSTG + b), 4 * KH);
     }
+    for (int x = 0; x < 8; ++x) mbar_init(ctx.bar(T::B_XCHG + x), 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -411,7 +439,14 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int blk = warp >> 2;                    // 0: block A, 1: block B
+    // KH warps per row: warp w works on block w / (4 KH) (A or B), on key
+    // part (w >> 2) % KH of every tile (HC = 128 / KH of its keys) and on
+    // the rows of TMEM lane quadrant w & 3.  With two parts the halves of a
+    // row share its running maximum (one exchange through shared memory per
+    // tile, so they take identical rescaling decisions) and each keeps its
+    // own part of the row sum until the end.
+    const int blk = warp / (4 * KH);              // 0: block A, 1: block B
+    const int half = (warp >> 2) % KH;            // key part of this warp
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;             // row within the Q block
     const bool live = blk == 0 || has_b;          // block B idles in a split item
@@ -422,8 +457,22 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + TM_S + 128 * blk;
     const uint32_t o_addr = tmem + lane_addr + TM_O + 128 * blk;
+    constexpr int OC = HD / 32 / KH;              // 32-column chunks of O per warp
+    float* xchg = reinterpret_cast<float*>(smem + T::OFF_XCHG);
+    auto xslot = [&](int par, int h) { return xchg + ((par * 2 + blk) * 2 + h) * BM + row; };
+    const int xbar = T::B_XCHG + blk * 4 + quad;  // the row halves' meeting point
+    // Publish this half's value in slot `par`, then read the other half's
+    // once both have arrived (phase `phase` of the meeting barrier).
+    auto exchange = [&](float mine, int par, int phase, float& theirs) {
+      *xslot(par, half) = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctx.bar(xbar));
+      if (!ctx.wait(xbar, phase & 1)) return false;
+      theirs = *xslot(par, half ^ 1);
+      return true;
+    };
     float m = -INFINITY;                          // reference max, log2 units
-    float l = 0.f;                                // running sum
+    float l = 0.f;                                // running sum (of this key part)
     bool ok = true;
     // ALiBi scales and biases the scores in place; the max and the
     // exponentials then take them as they are.
@@ -436,15 +485,19 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         break;
       }
       tc_fence_after();
-      float s[BN];
+      float s[HC];
       {
-        uint32_t r[BN];
-        tmem_ld128(s_addr, r);                    // the row's 128 scores in one round trip
+        uint32_t r[HC];
+        if constexpr (KH == 1)
+          tmem_ld128(s_addr, r);                  // the row's 128 scores in one round trip
+        else
+          tmem_ld64(s_addr + HC * half, r);       // this part's 64 scores
 #pragma unroll
-        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r[i]);
+        for (int i = 0; i < HC; ++i) s[i] = __uint_as_float(r[i]);
       }
+      const int key0 = j * BN + HC * half;        // key of column 0 of this part
       if constexpr (kAlibi) {
-        const float d0 = static_cast<float>(j * BN - q_row);   // key - query at column 0
+        const float d0 = static_cast<float>(key0 - q_row);   // key - query at column 0
         if (causal) {
           // every key the mask leaves has key <= query: -|i - j| = j - i;
           // on packed pairs: s = s scale + (slope c + slope d0)
@@ -452,13 +505,13 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
           const uint64_t slope2 = f2pack(slope_log2, slope_log2);
           const uint64_t scale2 = f2pack(scale_log2, scale_log2);
 #pragma unroll
-          for (int c = 0; c < BN; c += 2) {
+          for (int c = 0; c < HC; c += 2) {
             const uint64_t bias = f2fma(slope2, f2pack(static_cast<float>(c), static_cast<float>(c + 1)), base2);
             f2unpack(f2fma(f2pack(s[c], s[c + 1]), scale2, bias), s[c], s[c + 1]);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
+          for (int c = 0; c < HC; ++c)
             s[c] = fmaf(s[c], scale_log2, -slope_log2 * fabsf(d0 + static_cast<float>(c)));
         }
       }
@@ -473,9 +526,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         const int key_hi = causal ? min(q_row, N - 1) : (N - 1);
         const int key_lo = kWindow ? q_row - window + 1 : 0;
         const uint32_t span = static_cast<uint32_t>(key_hi - key_lo);
-        const int rel0 = j * BN - key_lo;
+        const int rel0 = key0 - key_lo;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
+        for (int c = 0; c < HC; ++c)
           if (static_cast<uint32_t>(rel0 + c) > span) s[c] = -INFINITY;
       }
       float mx;
@@ -487,18 +540,26 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
 #pragma unroll
         for (int k = 0; k < 8; ++k) mxp[k] = s[k];
 #pragma unroll
-        for (int c = 8; c < BN; c += 8)
+        for (int c = 8; c < HC; c += 8)
 #pragma unroll
           for (int k = 0; k < 8; ++k) mxp[k] = fmaxf(mxp[k], s[c + k]);
         mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                    fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       } else {
-        // three-input max: 64 instructions for the 128 scores (the softmax
-        // is bound by instruction issue, so each one saved counts)
+        // three-input max: one instruction per two scores (the softmax is
+        // bound by instruction issue, so each one saved counts)
         mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < BN; c += 2)
+        for (int c = 0; c < HC; c += 2)
           asm("max.f32 %0, %1, %2, %3;" : "=f"(mx) : "f"(mx), "f"(s[c]), "f"(s[c + 1]));
+      }
+      if constexpr (KH == 2) {
+        float other;
+        if (!exchange(mx, (j - lo) & 1, j - lo, other)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, other);
       }
       mx *= sl;
       // Raise the reference max only when the new one exceeds it by more
@@ -514,13 +575,14 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       // scores give exp2(-inf) = 0, not NaN.
       const float mref = (kWindow && m == -INFINITY) ? 0.f : m;
       // P = exp2(S scale - m) and the row sum
-      uint32_t pk[T::P_COLS];
+      constexpr int PW = T::P_COLS / KH;          // packed P words of this part
+      uint32_t pk[PW];
       // exponent arguments and row sums on packed fp32 pairs: one
       // instruction per two scores (measured +7% on the whole kernel)
       const uint64_t sl2 = f2pack(sl, sl), nm2 = f2pack(-mref, -mref);
       uint64_t acc2 = f2pack(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < BN / 4; ++c) {
+      for (int c = 0; c < HC / 4; ++c) {
         float a0, a1, a2, a3;
         f2unpack(f2fma(f2pack(s[4 * c], s[4 * c + 1]), sl2, nm2), a0, a1);
         f2unpack(f2fma(f2pack(s[4 * c + 2], s[4 * c + 3]), sl2, nm2), a2, a3);
@@ -532,13 +594,19 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       float r0, r1;
       f2unpack(acc2, r0, r1);
       l = l * corr + (r0 + r1);
-      // P (packed) over the first P_COLS columns of this block's S buffer
+      // Packed P of this part over its share of the first P_COLS columns of
+      // the block's S buffer.  With two parts the other one has read its
+      // scores from them already: it met this one after its load completed.
+      if constexpr (PW >= 32) {
 #pragma unroll
-      for (int c = 0; c < T::P_COLS; c += 32)
-        tmem_st32(s_addr + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+        for (int c = 0; c < PW; c += 32)
+          tmem_st32(s_addr + PW * half + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+      } else {
+        tmem_st16(s_addr + PW * half, pk);
+      }
       if (rescale_o) {
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = OC * half; c < OC * half + OC; ++c) {
           uint32_t r[32];
           tmem_ld32(o_addr + c * 32, r);
 #pragma unroll
@@ -552,9 +620,18 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       if (lane == 0) mbar_arrive(ctx.bar(T::B_PFULL + blk));
     }
 
+    // With two parts, the row sum of both (one more meeting).
+    float l_row = l;
+    if constexpr (KH == 2) {
+      if (ok && live) {
+        float other;
+        ok = exchange(l, (nt - lo) & 1, nt - lo, other);
+        l_row = l + other;
+      }
+    }
     if (ok && live && ctx.wait(T::B_ODONE + blk, 0)) {
       tc_fence_after();
-      const float inv_l = out_scale / l;
+      const float inv_l = out_scale / l_row;
       auto pack8 = [&](const uint32_t (&r)[32], int i) {
         return make_uint4(
             pack_bf16x2(__uint_as_float(r[8 * i]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
@@ -565,12 +642,12 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       if constexpr (T::kStoreTma) {
         // Every product of this block has completed, so its Q tile is free:
         // the row goes there in the tile's own swizzled layout (columns
-        // 32c.. of the row = 16-byte chunks 4(c&1).. of box c>>1), and one
-        // thread stores both boxes with the bulk tensor engine, which also
-        // drops the rows past N.
+        // 32c.. of the row = 16-byte chunks 4(c&1).. of box c>>1), each warp
+        // its OC chunks, and one thread stores both boxes with the bulk
+        // tensor engine, which also drops the rows past N.
         const uint32_t stage = blk ? T::OFF_QB : T::OFF_QA;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = OC * half; c < OC * half + OC; ++c) {
           uint32_t r[32];
           tmem_ld32(o_addr + c * 32, r);
           uint8_t* box = smem + stage + (c >> 1) * T::HALF;
@@ -581,7 +658,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(ctx.bar(T::B_OSTG + blk));
-        if (quad == 0 && lane == 0 && ctx.wait(T::B_OSTG + blk, 0)) {
+        if (quad == 0 && half == 0 && lane == 0 && ctx.wait(T::B_OSTG + blk, 0)) {
           tma_store_3d(tmO, sbase + stage, 0, qt * BM, bh);
           tma_store_3d(tmO, sbase + stage + T::HALF, 64, qt * BM, bh);
           bulk_commit_group();
@@ -590,7 +667,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       } else {
         __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q_row) * HD;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = OC * half; c < OC * half + OC; ++c) {
           uint32_t r[32];
           tmem_ld32(o_addr + c * 32, r);
           if (q_row < N) {
@@ -600,8 +677,8 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
           }
         }
       }
-      if (LSE != nullptr && q_row < N)
-        LSE[static_cast<size_t>(bh) * N + q_row] = m * kLn2 + logf(l);
+      if (LSE != nullptr && half == 0 && q_row < N)
+        LSE[static_cast<size_t>(bh) * N + q_row] = m * kLn2 + logf(l_row);
     }
   }
 
@@ -615,7 +692,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
 
 // kWindow: a sliding window is applied (window >= 1); kAlibi: ALiBi bias.
 template <bool kWindow, bool kAlibi>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(fwd_threads<kAlibi>(), 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                 __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int BH, int N,
@@ -627,7 +704,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 // Q, K e4m3 [BH, N, 128]; tmV maps the transposed copy V^T [BH, 128, keys].
 template <bool kWindow, bool kAlibi>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(fwd_threads<kAlibi>(), 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmVt, __nv_bfloat16* __restrict__ O,
                float* __restrict__ LSE, int BH, int N, float scale_log2, float v_descale,
@@ -739,7 +816,8 @@ cudaError_t launch_forward_bf16(const FwdMaps& maps, void* o, float* lse, int B,
   }
   const int head_group = forward_head_group(BH, H / Hkv, N, 2);
   if (ev.before) cudaEventRecord(ev.before, stream);
-  kernel<<<dim3(npair * BH + nsplit), dim3(NTHREADS), Bf16::SMEM_BYTES, stream>>>(
+  kernel<<<dim3(npair * BH + nsplit), dim3(alibi ? fwd_threads<true>() : fwd_threads<false>()),
+           Bf16::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.o, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2,
       causal, H / Hkv, window, alibi, H, nsplit, head_group);
   cudaError_t e = cudaGetLastError();
@@ -781,7 +859,8 @@ cudaError_t launch_forward_fp8(const FwdMaps& maps, void* o, float* lse, int B, 
                       : (window > 0 ? fwd_fp8_kernel<true, false> : fwd_fp8_kernel<false, false>);
   const int head_group = forward_head_group(BH, H / Hkv, N, 1);
   if (ev.before) cudaEventRecord(ev.before, stream);
-  kernel<<<dim3(npair * BH), dim3(NTHREADS), Fp8::SMEM_BYTES, stream>>>(
+  kernel<<<dim3(npair * BH), dim3(alibi ? fwd_threads<true>() : fwd_threads<false>()),
+           Fp8::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, static_cast<__nv_bfloat16*>(o), lse, BH, N, scale_log2, v_descale,
       causal, H / Hkv, window, alibi, H, head_group);
   cudaError_t e = cudaGetLastError();
