@@ -699,7 +699,10 @@ constexpr int DQ_NBAR = DQB_QTMEM + 1;
 constexpr uint32_t DQ_OFF_MISC = DQ_OFF_BAR + DQ_NBAR * 8;
 constexpr uint32_t DQ_SMEM = DQ_OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
 static_assert(DQ_SMEM <= 227u * 1024u, "dQ kernel shared memory exceeds the per-block limit");
-constexpr int DQ_THREADS = 352;                // 0-7 softmax, 8 producer, 9-10 MMA issuers
+// 0-7 softmax, 8 producer; MMA issuers 9 dQ, 10 S, 11 dP, each on its own SM
+// sub-partition (an issuing warp beside busy softmax warps gets ~80 cycles
+// per tcgen05.mma, so 16 products a tile from one warp set the pace)
+constexpr int DQ_THREADS = 384;
 constexpr uint32_t DQ_TM_DQ = 256;             // buffer x: S at 128x, dP at 128x + 64
 constexpr uint32_t DQ_TM_Q = 384;              // Q_i packed bf16: 64 columns
 constexpr uint32_t DQ_TM_DO = 448;             // dO_i packed bf16: 64 columns
@@ -802,9 +805,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------- dQ issuer
-    // dQ += dS K_t once the softmax of tile t is done; the score products
-    // come from warp 10 on another SM sub-partition (one thread issuing all
-    // of them shares its sub-partition's issue slots with two softmax warps).
+    // dQ += dS K_t once the softmax of tile t is done; S and dP come from
+    // warps 10 and 11, each on another SM sub-partition (one thread issuing
+    // every product shares its sub-partition's issue slots with two softmax
+    // warps and issues far below the tensor pipe's rate).
     if (lane == 0) {
       auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
       bool ok = true;
@@ -834,8 +838,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (ok) mma_commit(bar(DQB_DONE));
     }
     __syncwarp();
-  } else if (warp == 10) {
-    // ------------------------------------------------------- score issuer
+  } else if (warp == 10 || warp == 11) {
+    // ---------------------------------------------- score issuers (S, dP)
+    const bool dp = warp == 11;
     if (lane == 0) {
       auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
       auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
@@ -859,12 +864,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       bool ok = wait(DQB_QTMEM, 0);
       tc_fence_after();
       for (int t = 0; t < nt && ok; ++t) {
-        // buffer t & 1 holds dS(t - 2) until dQ(t - 2) has read it
-        if (t >= 2 && !(ok = wait(DQB_DSREAD + (t & 1), ((t - 2) >> 1) & 1))) break;
+        // The S columns of buffer t & 1 hold dS(t - 2) until dQ(t - 2) has
+        // read it; its dP columns hold dP(t - 2) until the softmax of tile
+        // t - 2 is done (it loads dP before it writes dS and arrives).
+        const uint32_t par = ((t - 2) >> 1) & 1;
+        if (t >= 2 && !(ok = wait((dp ? DQB_PFULL : DQB_DSREAD) + (t & 1), par))) break;
         if (!(ok = full(t))) break;
         tc_fence_after();
-        issue(t, false);
-        issue(t, true);
+        issue(t, dp);
       }
     }
     __syncwarp();
