@@ -326,8 +326,8 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
   if (deterministic) {                                            // 128-query blocks, 64-key tiles
     if (int r = make_map(&dq_maps.q, q, B * Hq, N, 128)) return r;
     if (int r = make_map(&dq_maps.dO, dO, B * Hq, N, 128)) return r;
-    if (int r = make_map(&dq_maps.k, k, B * Hkv, N, 64)) return r;
-    if (int r = make_map(&dq_maps.v, v, B * Hkv, N, 64)) return r;
+    if (int r = make_map(&dq_maps.k, k, B * Hkv, N, 128)) return r;
+    if (int r = make_map(&dq_maps.v, v, B * Hkv, N, 128)) return r;
   }
   if (own_ws) {
     if (workspace_alloc(&ws, need, stream) != cudaSuccess) {

@@ -661,52 +661,63 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 // ------------------------------------------------------------------ bwd_dq
 // Deterministic dQ (the dQ half of the gradient without atomics): one thread
-// block per (query head, 128-query block i), K_j / V_j streamed in 64-key
+// block per (query head, 128-query block i), K_j / V_j streamed in 128-key
 // tiles in increasing key order, dQ_i accumulated in TMEM and written once:
 //   S = Q_i K_j^T, dP = dO_i V_j^T            (Q_i, dO_i from TMEM)
 //   P = exp2(S scale log2e - LSE log2e [- ALiBi]),  dS = scale P * (dP - D)
-//   dQ_i += dS K_j                             (dS from TMEM, K_j MN-major)
+//   dQ_i += dS K_j                             (dS from shared memory, K_j MN-major)
 // Q_i and dO_i stay for the whole block, so they are copied into tensor
-// memory once and every product takes its A operand from there: per key
-// tile only K_j (twice) and V_j are read from shared memory.  Two TMEM
-// buffers of [S | dP] let the softmax of tile t overlap the products of
-// tiles t-1 and t+1.  Each dQ element is summed by one thread block in a
-// fixed order, so the result is the same on every run.
+// memory once and the score products take their A operand from there.  The
+// softmax copies S and dP into registers as soon as they land, so a single
+// TMEM region each suffices: the next tile's S and dP are computed while the
+// softmax still works on this one.  dS goes through shared memory to the dQ
+// product.  S, dP and dQ are issued by three warps on three SM
+// sub-partitions: an issuing warp beside busy softmax warps gets ~80 cycles
+// per tcgen05.mma, so 128-key tiles (half the instructions per FLOP of
+// 64-key ones) and one product kind per issuer keep issue off the critical
+// path.  Each dQ element is summed by one thread block in a fixed order, so
+// the result is the same on every run.
 constexpr int DQ_BQ = 128;                     // query rows (TMEM lanes)
-constexpr int DQ_BK = 64;                      // keys per tile
-constexpr int DQ_STAGES = 6;
-constexpr uint32_t DQ_QTILE = DQ_BQ * HD * 2;  // Q_i or dO_i: 32 KiB
-constexpr uint32_t DQ_QHALF = DQ_QTILE / 2;    // 128 rows x 64 columns
-constexpr uint32_t DQ_KTILE = DQ_BK * HD * 2;  // K_j or V_j: 16 KiB
-constexpr uint32_t DQ_KHALF = DQ_KTILE / 2;    // 64 rows x 64 columns
+constexpr int DQ_BK = 128;                     // keys per tile
+constexpr int DQ_STAGES = 3;
+constexpr uint32_t DQ_TILE = DQ_BQ * HD * 2;   // Q_i, dO_i, K_j or V_j: 32 KiB
+constexpr uint32_t DQ_HALF = DQ_TILE / 2;      // 128 rows x 64 columns (one swizzled box)
+constexpr uint32_t DQ_STAGE = 2 * DQ_TILE;     // K_j then V_j
 constexpr uint32_t DQ_OFF_RING = 0;
-// Q_i and dO_i land in the space of ring stages 4 and 5; once they have been
-// copied into tensor memory, that space joins the K/V ring.
-constexpr uint32_t DQ_OFF_Q = 4 * 2 * DQ_KTILE;
-constexpr uint32_t DQ_OFF_DO = DQ_OFF_Q + DQ_QTILE;
-constexpr uint32_t DQ_STAGE = 2 * DQ_KTILE;    // K_j then V_j
-constexpr uint32_t DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
+// Q_i and dO_i land in the space of ring stage 2; once they have been copied
+// into tensor memory, that space joins the K/V ring.
+constexpr uint32_t DQ_OFF_Q = 2 * DQ_STAGE;
+constexpr uint32_t DQ_OFF_DO = DQ_OFF_Q + DQ_TILE;
+constexpr uint32_t DQ_OFF_DS = DQ_STAGES * DQ_STAGE;   // dS [query][key]: two 64-key boxes
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DS + DQ_TILE;
 constexpr int DQB_QFULL = 0;
 constexpr int DQB_FULL = 1;                          // + stage
 constexpr int DQB_EMPTY = DQB_FULL + DQ_STAGES;      // + stage
-constexpr int DQB_SFULL = DQB_EMPTY + DQ_STAGES;     // + buffer: S(t) in TMEM
-constexpr int DQB_DPFULL = DQB_SFULL + 2;            // + buffer: dP(t) in TMEM
-constexpr int DQB_PFULL = DQB_DPFULL + 2;            // + buffer (8 warps)
-constexpr int DQB_DSREAD = DQB_PFULL + 2;            // + buffer: dQ(t) has read dS(t)
-constexpr int DQB_DONE = DQB_DSREAD + 2;
+constexpr int DQB_SFULL = DQB_EMPTY + DQ_STAGES;     // S(t) in TMEM
+constexpr int DQB_DPFULL = DQB_SFULL + 1;            // dP(t) in TMEM
+constexpr int DQB_SREAD = DQB_DPFULL + 1;            // the softmax has S(t) in registers (8 warps)
+constexpr int DQB_DPREAD = DQB_SREAD + 1;            // ... and dP(t) (8 warps)
+constexpr int DQB_PFULL = DQB_DPREAD + 1;            // dS(t) in shared memory (8 warps)
+constexpr int DQB_DSFREE = DQB_PFULL + 1;            // dQ(t) has read dS(t)
+constexpr int DQB_DONE = DQB_DSFREE + 1;
 constexpr int DQB_QTMEM = DQB_DONE + 1;              // Q_i, dO_i copied to TMEM (8 warps)
 constexpr int DQ_NBAR = DQB_QTMEM + 1;
 constexpr uint32_t DQ_OFF_MISC = DQ_OFF_BAR + DQ_NBAR * 8;
 constexpr uint32_t DQ_SMEM = DQ_OFF_MISC + 16 + 1024;   // + 1024-byte alignment slack
 static_assert(DQ_SMEM <= 227u * 1024u, "dQ kernel shared memory exceeds the per-block limit");
-// 0-7 softmax, 8 producer; MMA issuers 9 dQ, 10 S, 11 dP, each on its own SM
-// sub-partition (an issuing warp beside busy softmax warps gets ~80 cycles
-// per tcgen05.mma, so 16 products a tile from one warp set the pace)
-constexpr int DQ_THREADS = 384;
-constexpr uint32_t DQ_TM_DQ = 256;             // buffer x: S at 128x, dP at 128x + 64
+// 0-15 softmax (four per row, 32 keys each), 16 producer; MMA issuers 17 dQ,
+// 18 S, 19 dP
+constexpr int DQ_THREADS = 640;
+constexpr int DQ_SOFTMAX_WARPS = 16;
+constexpr int DQ_WARP_TMA = 16, DQ_WARP_DQ = 17, DQ_WARP_S = 18, DQ_WARP_DP = 19;
+constexpr uint32_t DQ_TM_S = 0;                // S: 128 columns
+constexpr uint32_t DQ_TM_DP = 128;             // dP: 128 columns
+constexpr uint32_t DQ_TM_DQ = 256;             // dQ accumulator: 128 columns
 constexpr uint32_t DQ_TM_Q = 384;              // Q_i packed bf16: 64 columns
 constexpr uint32_t DQ_TM_DO = 448;             // dO_i packed bf16: 64 columns
+// S, dP: M = 128 queries, N = 128 keys, A in TMEM, B K-major.
 constexpr uint32_t IDESC_DQ_S = idesc_bf16(DQ_BQ, DQ_BK, false, false);
+// dQ += dS K_j: M = 128 queries, N = d; A = dS K-major, B = K_j MN-major.
 constexpr uint32_t IDESC_DQ_ACC = idesc_bf16(DQ_BQ, HD, false, true);
 
 template <bool kAlibi>
@@ -747,6 +758,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int key_hi = causal ? min(N, q0 + DQ_BQ) : N;
   const int t_lo = key_lo / DQ_BK;
   const int nt = (key_hi + DQ_BK - 1) / DQ_BK - t_lo;
+  auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
+  auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(DQB_QFULL), 1);
@@ -754,18 +767,18 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(bar(DQB_FULL + s), 1);
       mbar_init(bar(DQB_EMPTY + s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(DQB_SFULL + x), 1);
-      mbar_init(bar(DQB_DPFULL + x), 1);
-      mbar_init(bar(DQB_PFULL + x), 8);
-      mbar_init(bar(DQB_DSREAD + x), 1);
-    }
+    mbar_init(bar(DQB_SFULL), 1);
+    mbar_init(bar(DQB_DPFULL), 1);
+    mbar_init(bar(DQB_SREAD), DQ_SOFTMAX_WARPS);
+    mbar_init(bar(DQB_DPREAD), DQ_SOFTMAX_WARPS);
+    mbar_init(bar(DQB_PFULL), DQ_SOFTMAX_WARPS);
+    mbar_init(bar(DQB_DSFREE), 1);
     mbar_init(bar(DQB_DONE), 1);
-    mbar_init(bar(DQB_QTMEM), 8);
+    mbar_init(bar(DQB_QTMEM), DQ_SOFTMAX_WARPS);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == DQ_WARP_DQ) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
@@ -774,7 +787,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == DQ_WARP_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -782,102 +795,86 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
       const uint32_t qf = bar(DQB_QFULL);
-      mbar_arrive_expect_tx(qf, 2 * DQ_QTILE);
+      mbar_arrive_expect_tx(qf, 2 * DQ_TILE);
       tma_load_3d(sbase + DQ_OFF_Q, &tmQ, qf, 0, q0, bh);
-      tma_load_3d(sbase + DQ_OFF_Q + DQ_QHALF, &tmQ, qf, 64, q0, bh);
+      tma_load_3d(sbase + DQ_OFF_Q + DQ_HALF, &tmQ, qf, 64, q0, bh);
       tma_load_3d(sbase + DQ_OFF_DO, &tmdO, qf, 0, q0, bh);
-      tma_load_3d(sbase + DQ_OFF_DO + DQ_QHALF, &tmdO, qf, 64, q0, bh);
+      tma_load_3d(sbase + DQ_OFF_DO + DQ_HALF, &tmdO, qf, 64, q0, bh);
       for (int t = 0; t < nt; ++t) {
         const int st = t % DQ_STAGES;
         if (t >= DQ_STAGES && !wait(DQB_EMPTY + st, ((t / DQ_STAGES) - 1) & 1)) break;
-        // stages 4 and 5 hold Q_i and dO_i until they are in tensor memory
-        if (t >= 4 && t < DQ_STAGES && !wait(DQB_QTMEM, 0)) break;
+        // stage 2 holds Q_i and dO_i until they are in tensor memory
+        if (t == 2 && !wait(DQB_QTMEM, 0)) break;
         const uint32_t fb = bar(DQB_FULL + st);
-        const uint32_t dst = sbase + DQ_OFF_RING + st * DQ_STAGE;
+        const uint32_t dst = ring(t);
         const int key = (t_lo + t) * DQ_BK;
         mbar_arrive_expect_tx(fb, DQ_STAGE);
         tma_load_3d(dst, &tmK, fb, 0, key, bkv);
-        tma_load_3d(dst + DQ_KHALF, &tmK, fb, 64, key, bkv);
-        tma_load_3d(dst + DQ_KTILE, &tmV, fb, 0, key, bkv);
-        tma_load_3d(dst + DQ_KTILE + DQ_KHALF, &tmV, fb, 64, key, bkv);
+        tma_load_3d(dst + DQ_HALF, &tmK, fb, 64, key, bkv);
+        tma_load_3d(dst + DQ_TILE, &tmV, fb, 0, key, bkv);
+        tma_load_3d(dst + DQ_TILE + DQ_HALF, &tmV, fb, 64, key, bkv);
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == DQ_WARP_DQ) {
     // ------------------------------------------------------- dQ issuer
-    // dQ += dS K_t once the softmax of tile t is done; S and dP come from
-    // warps 10 and 11, each on another SM sub-partition (one thread issuing
-    // every product shares its sub-partition's issue slots with two softmax
-    // warps and issues far below the tensor pipe's rate).
+    // dQ += dS K_t once the softmax of tile t has written dS: A = dS from
+    // shared memory (K-major: two 64-key boxes), B = K_t MN-major (16 keys =
+    // 2048 bytes per step, the two 64-column blocks of d 16 KiB apart).
     if (lane == 0) {
-      auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
+      const uint64_t dsd = sdesc_sw128(sbase + DQ_OFF_DS, 16, 1024);
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
-        const int x = t & 1;
-        if (!(ok = wait(DQB_PFULL + x, (t >> 1) & 1))) break;
+        if (!(ok = wait(DQB_PFULL, t & 1))) break;
         tc_fence_after();
-        // dQ += dS K_t: dS packed in TMEM (keys 0-31 in columns [0, 16),
-        // keys 32-63 in [32, 48) of the buffer), K_t MN-major (16 keys =
-        // 2048 bytes per step, 64-column blocks 8 KiB apart).
-        {
-          const uint64_t kd = sdesc_sw128(ring(t), DQ_KHALF, 1024);
-          uint32_t a[4];
-          uint64_t b[4];
+        const uint64_t kd = sdesc_sw128(ring(t), DQ_HALF, 1024);
+        uint64_t a[8], b[8];
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            a[kk] = tmem + 128u * x + 32 * (kk >> 1) + 8 * (kk & 1);
-            b[kk] = kd + ((kk * 2048) >> 4);
-          }
-          mma_ts_batch4(tmem + DQ_TM_DQ, a, b, IDESC_DQ_ACC, t > 0 ? 1u : 0u);
+        for (int kk = 0; kk < DQ_BK / 16; ++kk) {
+          a[kk] = dsd + (((kk >> 2) * DQ_HALF + (kk & 3) * 32) >> 4);
+          b[kk] = kd + ((kk * 2048) >> 4);
         }
-        // S(t), dP(t) completed before the softmax of tile t, so this covers
-        // every reader of stage t and of buffer x's dS.
+        mma_ss_batch8(tmem + DQ_TM_DQ, a, b, IDESC_DQ_ACC, t > 0 ? 1u : 0u);
+        // S(t) and dP(t) completed before the softmax of tile t wrote dS,
+        // so this covers every reader of stage t; and of dS(t).
         mma_commit(bar(DQB_EMPTY + t % DQ_STAGES));
-        mma_commit(bar(DQB_DSREAD + x));
+        mma_commit(bar(DQB_DSFREE));
       }
       if (ok) mma_commit(bar(DQB_DONE));
     }
     __syncwarp();
-  } else if (warp == 10 || warp == 11) {
+  } else if (warp == DQ_WARP_S || warp == DQ_WARP_DP) {
     // ---------------------------------------------- score issuers (S, dP)
-    const bool dp = warp == 11;
+    // S(t) = Q_i K_t^T or dP(t) = dO_i V_t^T (one warp each): A from
+    // TMEM (16 elements of d = 8 packed columns per step), B = the K or V
+    // tile K-major.  Each waits for the softmax to have copied its previous
+    // result into registers.
+    const bool dp = warp == DQ_WARP_DP;
     if (lane == 0) {
-      auto ring = [&](int t) { return sbase + DQ_OFF_RING + (t % DQ_STAGES) * DQ_STAGE; };
-      auto full = [&](int t) { return wait(DQB_FULL + t % DQ_STAGES, (t / DQ_STAGES) & 1); };
-      // S(t) into buffer t & 1 and dP(t) beside it: reductions over d, each
-      // committed to its own barrier so that the exponentials start while
-      // dP(t) is still on its way.  A (Q_i or dO_i) comes from TMEM, 16
-      // elements of d = 8 packed columns per step.
-      auto issue = [&](int t, bool dp) {
-        const uint32_t buf = tmem + 128u * (t & 1) + (dp ? 64u : 0u);
-        const uint64_t bd = sdesc_sw128(ring(t) + (dp ? DQ_KTILE : 0u), 16, 1024);
+      bool ok = wait(DQB_QTMEM, 0);
+      tc_fence_after();
+      for (int t = 0; t < nt && ok; ++t) {
+        if (t >= 1 && !(ok = wait(dp ? DQB_DPREAD : DQB_SREAD, (t - 1) & 1))) break;
+        if (!(ok = full(t))) break;
+        tc_fence_after();
+        const uint64_t bd = sdesc_sw128(ring(t) + (dp ? DQ_TILE : 0u), 16, 1024);
         uint32_t a[8];
         uint64_t b[8];
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           a[kk] = tmem + (dp ? DQ_TM_DO : DQ_TM_Q) + 8 * kk;
-          b[kk] = bd + (((kk >> 2) * DQ_KHALF + (kk & 3) * 32) >> 4);
+          b[kk] = bd + (((kk >> 2) * DQ_HALF + (kk & 3) * 32) >> 4);
         }
-        mma_ts_batch8(buf, a, b, IDESC_DQ_S, 0u);
-        mma_commit(bar((dp ? DQB_DPFULL : DQB_SFULL) + (t & 1)));
-      };
-      bool ok = wait(DQB_QTMEM, 0);
-      tc_fence_after();
-      for (int t = 0; t < nt && ok; ++t) {
-        // The S columns of buffer t & 1 hold dS(t - 2) until dQ(t - 2) has
-        // read it; its dP columns hold dP(t - 2) until the softmax of tile
-        // t - 2 is done (it loads dP before it writes dS and arrives).
-        const uint32_t par = ((t - 2) >> 1) & 1;
-        if (t >= 2 && !(ok = wait((dp ? DQB_PFULL : DQB_DSREAD) + (t & 1), par))) break;
-        if (!(ok = full(t))) break;
-        tc_fence_after();
-        issue(t, dp);
+        mma_ts_batch8(tmem + (dp ? DQ_TM_DP : DQ_TM_S), a, b, IDESC_DQ_S, 0u);
+        mma_commit(bar(dp ? DQB_DPFULL : DQB_SFULL));
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    // Warp w: TMEM lane quadrant w & 3 (query rows), key half w >> 2.
+    // Warp w: TMEM lane quadrant w & 3 (query rows), key quarter w >> 2 (32
+    // of the tile's 128 keys).  Four warps per row: each one's serial work
+    // per tile (load, exponentials, dS) is a quarter of a row.
     const int quad = warp & 3, sub = warp >> 2;
     const int row = quad * 32 + lane;
     const int q = q0 + row;
@@ -891,18 +888,19 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // keys this row sees: [lo, hi]
     const int lo = window > 0 ? q - window + 1 : 0;
     const int hi = causal ? min(q, N - 1) : N - 1;
-    // Q_i (warps 0-3) or dO_i (warps 4-7), row by row, into tensor memory:
-    // column c holds elements 2c and 2c+1 of the row (the A-operand layout).
+    // Q_i (warps 0-7) or dO_i (warps 8-15), row by row, into tensor memory,
+    // half a row (one 64-column box) per warp: column c holds elements 2c
+    // and 2c+1 of the row (the A-operand layout).
     bool ok = wait(DQB_QFULL, 0);
     if (ok) {
-      const uint8_t* tile = smem + (sub == 0 ? DQ_OFF_Q : DQ_OFF_DO);
-      const uint32_t col = sub == 0 ? DQ_TM_Q : DQ_TM_DO;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      const uint8_t* tile = smem + (sub < 2 ? DQ_OFF_Q : DQ_OFF_DO);
+      const uint32_t col = sub < 2 ? DQ_TM_Q : DQ_TM_DO;
+      {
+        const int h = sub & 1;
         uint32_t r[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(tile + h * DQ_QHALF +
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + h * DQ_HALF +
                                                           sw128_offset(row, c));
           r[4 * c] = v.x;
           r[4 * c + 1] = v.y;
@@ -917,28 +915,35 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(DQB_QTMEM));
     }
+    const uint32_t s_addr = tmem + lane_addr + DQ_TM_S + 32 * sub;
+    const uint32_t dp_addr = tmem + lane_addr + DQ_TM_DP + 32 * sub;
+    uint8_t* ds_box = smem + DQ_OFF_DS + (sub >> 1) * DQ_HALF;   // box of this warp's 32 keys
+    const uint64_t sc2 = f2pack(scale_log2, scale_log2);
+    const uint64_t s2 = f2pack(scale, scale), nd2 = f2pack(nd, nd);
     for (int t = 0; t < nt && ok; ++t) {
-      const int x = t & 1;
-      if (!wait(DQB_SFULL + x, (t >> 1) & 1)) {
+      if (!wait(DQB_SFULL, t & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + 128u * x + 32 * sub;
-      const int j0 = (t_lo + t) * DQ_BK + 32 * sub;               // first key of this half
+      const int j0 = (t_lo + t) * DQ_BK + 32 * sub;               // first key of this quarter
       const bool need_mask = !row_valid || j0 < lo || j0 + 31 > hi;
       const float d0 = static_cast<float>(q - j0);
       float p[32];
       {
         uint32_t sr[32];
-        tmem_ld32(s_addr, sr);
-        const uint64_t sc2 = f2pack(scale_log2, scale_log2);
+        tmem_ld32(s_addr, sr);                    // this quarter's 32 scores
+        // S(t) is in registers: its columns may take S(t + 1)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(DQB_SREAD));
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
+          const int k = e;
           float b0 = nlse, b1 = nlse;
           if constexpr (kAlibi) {
-            b0 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e)), nlse);
-            b1 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(e + 1)), nlse);
+            b0 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(k)), nlse);
+            b1 = fmaf(-slope_log2, fabsf(d0 - static_cast<float>(k + 1)), nlse);
           }
           // exponent arguments on a packed fp32 pair
           float a0, a1;
@@ -947,16 +952,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           float p0 = fast_exp2(a0);
           float p1 = fast_exp2(a1);
           if (need_mask) {
-            const bool v0 = row_valid && j0 + e >= lo && j0 + e <= hi;
-            const bool v1 = row_valid && j0 + e + 1 >= lo && j0 + e + 1 <= hi;
+            const bool v0 = row_valid && j0 + k >= lo && j0 + k <= hi;
+            const bool v1 = row_valid && j0 + k + 1 >= lo && j0 + k + 1 <= hi;
             p0 = v0 ? p0 : 0.f;
             p1 = v1 ? p1 : 0.f;
           }
-          p[e] = p0;
-          p[e + 1] = p1;
+          p[k] = p0;
+          p[k + 1] = p1;
         }
       }
-      if (!wait(DQB_DPFULL + x, (t >> 1) & 1)) {
+      if (!wait(DQB_DPFULL, t & 1)) {
         ok = false;
         break;
       }
@@ -964,34 +969,44 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t gk[16];
       {
         uint32_t dr[32];
-        tmem_ld32(s_addr + 64, dr);
-        const uint64_t s2 = f2pack(scale, scale), nd2 = f2pack(nd, nd);
+        tmem_ld32(dp_addr, dr);
+        // dP(t) is in registers: its columns may take dP(t + 1)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(DQB_DPREAD));
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
+          const int k = e;
           // scale dS = P (scale dP - scale D) on a packed fp32 pair
           float g0, g1;
-          f2unpack(f2mul(f2pack(p[e], p[e + 1]),
+          f2unpack(f2mul(f2pack(p[k], p[k + 1]),
                          f2fma(f2pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), s2,
                                nd2)), g0, g1);
-          gk[e / 2] = pack_bf16x2(g0, g1);
+          gk[k / 2] = pack_bf16x2(g0, g1);
         }
       }
-      // packed dS over the first 16 of the 32 columns this thread just read
-      tmem_st16(s_addr, gk);
-      tmem_wait_st();
-      tc_fence_before();
+      // dS row into shared memory (the K-major A operand of dQ) once dQ(t-1)
+      // has read the previous one
+      if (t >= 1 && !wait(DQB_DSFREE, (t - 1) & 1)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(ds_box + sw128_offset(row, 4 * (sub & 1) + c)) =
+            make_uint4(gk[4 * c], gk[4 * c + 1], gk[4 * c + 2], gk[4 * c + 3]);
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(DQB_PFULL + x));
+      if (lane == 0) mbar_arrive(bar(DQB_PFULL));
     }
     if (ok && wait(DQB_DONE, 0)) {
       tc_fence_after();
-      __nv_bfloat16* out = dQ + (static_cast<size_t>(bh) * N + q) * HD + 64 * sub;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      __nv_bfloat16* out = dQ + (static_cast<size_t>(bh) * N + q) * HD + 32 * sub;
+      {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + DQ_TM_DQ + 64 * sub + 32 * c, r);
+        tmem_ld32(tmem + lane_addr + DQ_TM_DQ + 32 * sub, r);
         if (row_valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(out + 32 * c);
+          uint4* d4 = reinterpret_cast<uint4*>(out);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             d4[i] = make_uint4(
@@ -1006,7 +1021,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == DQ_WARP_DQ) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
