@@ -97,12 +97,16 @@ constexpr uint32_t TMEM_COLS = 512;
 // buffer X: R0 = [128 X, 128 X + 64), R1 = [128 X + 64, 128 X + 128)
 constexpr uint32_t TM_DV = 256, TM_DK = 384;
 
-// 0-7 softmax, 8-11 dQ writers, 12 producer; MMA issuers: 13 dV/dK, 14 S^T/dP^T, 15 dQ^T
-constexpr int NTHREADS = 512;
-constexpr int WARP_TMA = 12;
-constexpr int WARP_MMA = 13;
-constexpr int WARP_MMA2 = 14;
-constexpr int WARP_MMA3 = 15;
+// Warps: 0-7 softmax, then the dQ writers (eight, two per TMEM lane quadrant
+// and 32 queries each, when this kernel forms dQ; none otherwise), then the
+// producer and the MMA issuers (dV/dK, S^T/dP^T, dQ^T), which land on SM
+// sub-partitions 0, 1, 2, 3 either way.  The fp32 reductions of dQ are
+// bound by how many a warp keeps in flight (measured on this GPU: ~11 B/clk
+// per SM with four warps issuing them, ~18 with eight).
+template <bool kDq>
+__host__ __device__ constexpr int bwd_writers() { return kDq ? 8 : 0; }
+template <bool kDq>
+__host__ __device__ constexpr int bwd_threads() { return 32 * (12 + bwd_writers<kDq>()); }
 // Key/value heads whose thread blocks are ordered together: 8, fewer when
 // the query rows they serve (Q, dO and the fp32 dQ accumulator: 1 KiB per
 // row, g query heads per key/value head) pass ~128 MB of L2.
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const float* __restric
 // modulo heads).  kDq: this kernel also forms dQ (fp32 atomics into dq_acc);
 // without it only dK and dV are made and dQ is left to bwd_dq_kernel.
 template <bool kAlibi, bool kDq>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(bwd_threads<kDq>(), 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -217,6 +221,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int WARP_TMA = 8 + bwd_writers<kDq>();
+  constexpr int WARP_MMA = WARP_TMA + 1;    // dV/dK
+  constexpr int WARP_MMA2 = WARP_TMA + 2;   // S^T/dP^T
+  constexpr int WARP_MMA3 = WARP_TMA + 3;   // dQ^T
   // Blocks are ordered by groups of head_group key/value heads, so the few
   // heads in flight keep their dQ accumulator, Q and dO resident in L2;
   // within a group, key blocks go in increasing order (most work first when
@@ -259,7 +267,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mbar_init(bar_addr(sbase, B_DPFULL + x), 1);
       mbar_init(bar_addr(sbase, B_PFULL + x), 8);
       mbar_init(bar_addr(sbase, B_DQFULL + x), 1);
-      mbar_init(bar_addr(sbase, B_DQFREE + x), 4);
+      mbar_init(bar_addr(sbase, B_DQFREE + x), 8);
       mbar_init(bar_addr(sbase, B_DKV + x), 1);
     }
     mbar_init(bar_addr(sbase, B_DONE), 1);
@@ -620,21 +628,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (kDq && warp < WARP_TMA) {
     // ------------------------------------------------------------ dQ writers
     const int quad = warp & 3;
+    const int wq = (warp - 8) >> 2;                  // query half of this writer
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;   // lane = d index
     Cursor cur = first;
     for (int it = 0; it < nit; ++it, cur.next(i0, i1)) {
       const int x = it & 1;
-      const int qb = cur.qi * BQ;
+      const int qb = cur.qi * BQ + 32 * wq;          // first query of this writer's half
       const int bh = cur.hq;
       if (!ctx.wait(B_DQFULL + x, (it >> 1) & 1)) break;
       tc_fence_after();
-      float g[BQ];
-#pragma unroll
-      for (int c = 0; c < BQ / 32; ++c) {
+      float g[32];
+      {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + 128u * x + 64 + c * 32, r);
+        tmem_ld32(tmem + lane_addr + 128u * x + 64 + 32 * wq, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[c * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) g[i] = __uint_as_float(r[i]);
       }
       tc_fence_before();
       __syncwarp();
@@ -643,10 +651,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // row's 32 entries of this quadrant: 128 contiguous bytes, no shuffles
       // (fewer issue slots taken beside the MMA-issuing warp than the 4x4
       // register transpose that 16-byte vector atomics need).
-      const int lim = min(BQ, N - qb);
+      const int lim = min(32, N - qb);
       float* base = dq_acc + (static_cast<size_t>(bh) * N + qb) * HD + quad * 32 + lane;
 #pragma unroll
-      for (int q = 0; q < BQ; ++q)
+      for (int q = 0; q < 32; ++q)
         if (q < lim) red_add(base + static_cast<size_t>(q) * HD, g[q]);
     }
   }
@@ -1093,7 +1101,8 @@ cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void*
   auto kernel = deterministic
                     ? (alibi ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>)
                     : (alibi ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>);
-  kernel<<<dim3(nkv * B * Hkv), dim3(NTHREADS), SMEM_BYTES, stream>>>(
+  kernel<<<dim3(nkv * B * Hkv), dim3(deterministic ? bwd_threads<false>() : bwd_threads<true>()),
+           SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.dO, maps.dk, maps.dv, lse_pad, d_pad, dq_acc, B * Hkv, N,
       Npad, scale, causal, g, window, head_group, alibi, H);
   e = cudaGetLastError();
