@@ -334,7 +334,9 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       if (has_b) T::load_rows(sbase + T::OFF_QB, tmQ, qf, q0 + BM, bh);
       bool ok = true;
       int cnt = 0;
-      for (int j = loA; j < ntB && ok; ++j) {
+      // key tiles in processing order: the last one (the diagonal one when
+      // causal) first, down to loA
+      for (int j = ntB - 1; j >= loA && ok; --j) {
         for (int which = 0; which < 2 && ok; ++which, ++cnt) {
           const int slot = cnt % SLOTS;
           if (cnt >= SLOTS && !ctx.wait(T::B_EMPTY + slot, ((cnt / SLOTS) - 1) & 1)) {
@@ -355,65 +357,70 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // Tiles are numbered from loA: K_j sits in slot (2t) % SLOTS and V_j in
-      // (2t+1) % SLOTS with t = j - loA; the n-th fill of a slot completes
-      // phase n of its FULL barrier.  Block A works on tiles [loA, ntA) and
-      // block B on [loB, ntB), with loB <= loA + 1 and ntB >= ntA, so B takes
-      // every tile after the first.
-      auto full_k = [&](int j) {
-        const int t = j - loA;
+      // Key tiles go in decreasing order: step t works on tile ntB - 1 - t,
+      // K in slot (2t) % SLOTS and V in (2t+1) % SLOTS; the n-th fill of a
+      // slot completes phase n of its FULL barrier.  Block B (the later Q
+      // tile) works on steps [0, tB1], block A on [tA0, nsteps): under the
+      // causal mask the step that only block B needs (its diagonal tile) is
+      // the first one, where the pipeline is filling anyway, and both blocks
+      // end together on tile loA instead of block A's softmax idling through
+      // block B's last tile.
+      const int nsteps = ntB - loA;
+      const int tA0 = ntB - ntA;
+      const int tB1 = ntB - 1 - loB;
+      auto full_k = [&](int t) {
         return ctx.wait(T::B_FULL + (2 * t) % SLOTS, ((2 * t) / SLOTS) & 1);
       };
-      auto full_v = [&](int j) {
-        const int t = j - loA;
+      auto full_v = [&](int t) {
         return ctx.wait(T::B_FULL + (2 * t + 1) % SLOTS, ((2 * t + 1) / SLOTS) & 1);
       };
-      auto active_a = [&](int j) { return j < ntA; };
-      auto active_b = [&](int j) { return has_b && j >= loB; };
-      bool ok = ctx.wait(T::B_QFULL, 0) && full_k(loA);
+      auto active_a = [&](int t) { return t >= tA0 && t < nsteps; };
+      auto active_b = [&](int t) { return has_b && t <= tB1; };
+      bool ok = ctx.wait(T::B_QFULL, 0) && full_k(0);
       if (ok) {
         tc_fence_after();
-        T::issue_s(tmem + TM_S, sbase + T::OFF_QA, sbase + T::OFF_SLOT);
-        mma_commit(ctx.bar(T::B_SFULL + 0));
-        if (active_b(loA)) {
+        if (active_a(0)) {
+          T::issue_s(tmem + TM_S, sbase + T::OFF_QA, sbase + T::OFF_SLOT);
+          mma_commit(ctx.bar(T::B_SFULL + 0));
+        }
+        if (active_b(0)) {
           T::issue_s(tmem + TM_S + 128, sbase + T::OFF_QB, sbase + T::OFF_SLOT);
           mma_commit(ctx.bar(T::B_SFULL + 1));
         }
         mma_commit(ctx.bar(T::B_EMPTY + 0));
       }
-      for (int j = loA; j < ntB && ok; ++j) {
-        const int t = j - loA;
+      for (int t = 0; t < nsteps && ok; ++t) {
         const int vslot = (2 * t + 1) % SLOTS;
         const int kslot_next = (2 * t + 2) % SLOTS;
         bool v_ready = false, k_next_ready = false;
-        if (active_a(j)) {
-          ok = ctx.wait(T::B_PFULL + 0, (j - loA) & 1) && full_v(j);
+        if (active_a(t)) {
+          ok = ctx.wait(T::B_PFULL + 0, (t - tA0) & 1) && full_v(t);
           if (!ok) break;
           v_ready = true;
           tc_fence_after();
-          T::issue_pv(tmem + TM_O, tmem + TM_S, sbase + T::OFF_SLOT + vslot * T::TILE, j == loA);
-          if (j == ntA - 1) mma_commit(ctx.bar(T::B_ODONE + 0));
+          T::issue_pv(tmem + TM_O, tmem + TM_S, sbase + T::OFF_SLOT + vslot * T::TILE, t == tA0);
+          if (t == nsteps - 1) mma_commit(ctx.bar(T::B_ODONE + 0));
         }
-        if (active_a(j + 1)) {
-          ok = full_k(j + 1);
+        if (active_a(t + 1)) {
+          ok = full_k(t + 1);
           if (!ok) break;
           k_next_ready = true;
           tc_fence_after();
           T::issue_s(tmem + TM_S, sbase + T::OFF_QA, sbase + T::OFF_SLOT + kslot_next * T::TILE);
           mma_commit(ctx.bar(T::B_SFULL + 0));
         }
-        if (active_b(j)) {
-          ok = ctx.wait(T::B_PFULL + 1, (j - loB) & 1) && (v_ready || full_v(j));
+        if (active_b(t)) {
+          ok = ctx.wait(T::B_PFULL + 1, t & 1) && (v_ready || full_v(t));
           if (!ok) break;
           tc_fence_after();
-          T::issue_pv(tmem + TM_O + 128, tmem + TM_S + 128, sbase + T::OFF_SLOT + vslot * T::TILE, j == loB);
-          if (j == ntB - 1) mma_commit(ctx.bar(T::B_ODONE + 1));
+          T::issue_pv(tmem + TM_O + 128, tmem + TM_S + 128, sbase + T::OFF_SLOT + vslot * T::TILE, t == 0);
+          if (t == tB1) mma_commit(ctx.bar(T::B_ODONE + 1));
         }
         mma_commit(ctx.bar(T::B_EMPTY + vslot));
-        if (j + 1 < ntB) {
-          ok = k_next_ready || full_k(j + 1);
+        if (t + 1 < nsteps) {
+          ok = k_next_ready || full_k(t + 1);
           if (!ok) break;
-          if (has_b) {
+          if (active_b(t + 1)) {
             tc_fence_after();
             T::issue_s(tmem + TM_S + 128, sbase + T::OFF_QB,
                        sbase + T::OFF_SLOT + kslot_next * T::TILE);
@@ -466,8 +473,10 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
     const float slope_log2 = kAlibi ? alibi[bh % heads] * 1.4426950408889634f : 0.f;
     const float sl = kAlibi ? 1.f : scale_log2;
 
-    for (int j = lo; j < nt; ++j) {
-      if (!ctx.wait(T::B_SFULL + blk, (j - lo) & 1)) {
+    // this block's key tiles, last first (the order the products come in)
+    for (int u = 0; u < nt - lo; ++u) {
+      const int j = nt - 1 - u;
+      if (!ctx.wait(T::B_SFULL + blk, u & 1)) {
         ok = false;
         break;
       }
@@ -542,7 +551,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
       }
       if constexpr (KH == 2) {
         float other;
-        if (!exchange(mx, (j - lo) & 1, j - lo, other)) {
+        if (!exchange(mx, u & 1, u, other)) {
           ok = false;
           break;
         }
@@ -556,7 +565,7 @@ __device__ __forceinline__ void fwd_body(const CUtensorMap* tmQ, const CUtensorM
         corr = fast_exp2(m - mx);                 // 0 on the first tile
         m = mx;
       }
-      const bool rescale_o = (j > lo) && __any_sync(0xffffffffu, corr != 1.f);
+      const bool rescale_o = (u > 0) && __any_sync(0xffffffffu, corr != 1.f);
       // A row that has seen no visible key yet (only possible with a window)
       // keeps m = -inf; it uses 0 as the exponent reference so its masked
       // scores give exp2(-inf) = 0, not NaN.
