@@ -32,7 +32,7 @@
 //                i+1.  Three warps issue the products, each on its own SM
 //                sub-partition (S^T/dP^T, dV/dK, dQ^T), so the issue slots
 //                that the softmax and writer warps take on one do not stall
-//                the others.  Four writer warps add dQ_i into the fp32
+//                the others.  Eight writer warps add dQ_i into the fp32
 //                accumulator with fp32 atomics (one warp instruction covers
 //                one query row's 128 contiguous bytes of its quadrant).  dK
 //                and dV leave TMEM once.
@@ -84,7 +84,7 @@ constexpr int B_SFULL = B_QEMPTY + STAGES; // + buffer: S^T in TMEM
 constexpr int B_DPFULL = B_SFULL + 2;      // + buffer: dP^T in TMEM
 constexpr int B_PFULL = B_DPFULL + 2;      // + buffer: P^T, dS^T written (8 warps)
 constexpr int B_DQFULL = B_PFULL + 2;      // + buffer
-constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 4 writer warps read dQ^T
+constexpr int B_DQFREE = B_DQFULL + 2;     // + buffer: 8 writer warps read dQ^T
 constexpr int B_DKV = B_DQFREE + 2;       // + buffer: dV/dK(i) have read R0_X
 constexpr int B_DONE = B_DKV + 2;          // the dV/dK issuer's products completed
 constexpr int B_DONE3 = B_DONE + 1;        // dQ issuer's products completed
