@@ -323,7 +323,7 @@ static int backward_impl(const char* fn, const void* q, const void* k, const voi
   if (int r = make_map(&maps.v, v, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.dk, dk, B * Hkv, N, 128)) return r;
   if (int r = make_map(&maps.dv, dv, B * Hkv, N, 128)) return r;
-  if (deterministic) {                                            // 128-query blocks, 64-key tiles
+  if (deterministic) {                                            // 128-query and 128-key tiles
     if (int r = make_map(&dq_maps.q, q, B * Hq, N, 128)) return r;
     if (int r = make_map(&dq_maps.dO, dO, B * Hq, N, 128)) return r;
     if (int r = make_map(&dq_maps.k, k, B * Hkv, N, 128)) return r;

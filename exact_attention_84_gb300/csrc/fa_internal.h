@@ -55,7 +55,7 @@ struct BwdMaps {
 size_t backward_workspace_bytes(int B, int H, int N);
 // Q, dO, O, LSE, dQ have H query heads; K, V, dK, dV have Hkv (H % Hkv == 0).
 // maps: Q, dO with 64-row boxes, K, V, dK, dV with 128-row boxes.  dq_maps: nullptr,
-// or (deterministic dQ) Q, dO with 128-row boxes and K, V with 64-row boxes.
+// or (deterministic dQ) Q, dO, K and V with 128-row boxes.
 cudaError_t launch_backward_bf16(const BwdMaps& maps, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,
                                  const void* dO, void* dq, void* dk, void* dv, int B, int H,
