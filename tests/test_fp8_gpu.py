@@ -138,21 +138,30 @@ def test_fp8_uniform_v():
     check_fp8(o, lse, q8, k8, v8, SCALE, True, 0, (DS, DS, 0.5), "uniform V")
 
 
-def test_fp8_long_causal_n8192_sampled():
+def test_fp8_long_causal_n8192_every_element():
+    """The fp8 workload (B1 H32 N8192, causal) in full: every element of
+    every head within the bound above, the mean over all of them within the
+    mean limit, every LSE within 1e-3.  Head by head, so the host holds one
+    8192 x 8192 score matrix at a time."""
     w = inputs.FP8_LONG_CAUSAL
     q8, k8, v8 = inputs.workload_inputs(w, "cuda")
     o, lse = api.forward_fp8(q8, k8, v8, DS, DS, DS, causal=True, scale=SCALE)
-    rng = np.random.default_rng(8)
-    rows = np.unique(np.concatenate([np.arange(32), np.arange(w.N - 32, w.N),
-                                     rng.choice(w.N, 96, replace=False)]))
-    for h in (0, 17, 31):
-        qd = f8.decode_e4m3(q8[0, h].cpu().numpy()) * DS
-        kd = f8.decode_e4m3(k8[0, h].cpu().numpy()) * DS
-        vd = f8.decode_e4m3(v8[0, h].cpu().numpy())
-        o_ref, lse_ref = orc.attention_forward_rows(qd[rows], kd, vd * DS, rows, SCALE, True)
-        got = np64(o[0, h, rows])
-        err = np.abs(got - o_ref)
-        bound, sig = fp8_bound(qd[rows], kd, vd, o_ref, SCALE, True, 0, DS, rows=rows)
+    O, LSE = np64(o), np64(lse)
+    q8n, k8n, v8n = (t.cpu().numpy() for t in (q8, k8, v8))
+    err_sum = sig_sum = ref_sum = 0.0
+    for h in range(w.H):
+        sl = slice(h, h + 1)
+        o_ref, lse_ref = f8.attention_forward_fp8(q8n[:, sl], k8n[:, sl], v8n[:, sl], SCALE,
+                                                  DS, DS, DS, True, None)
+        qd = f8.decode_e4m3(q8n[0, h]) * DS
+        kd = f8.decode_e4m3(k8n[0, h]) * DS
+        vd = f8.decode_e4m3(v8n[0, h])
+        err = np.abs(O[0, h] - o_ref[0, 0])
+        bound, sig = fp8_bound(qd, kd, vd, o_ref[0, 0], SCALE, True, 0, DS)
         assert (err <= bound).all(), f"head {h}: x{(err / bound).max():.2f} over the bound"
-        assert err.mean() <= sig.mean() + 2.0 ** -9 * np.abs(o_ref).mean() + 1e-5
-        assert np.abs(np64(lse[0, h, rows]) - lse_ref).max() <= LSE_MAX
+        assert np.abs(LSE[0, h] - lse_ref[0, 0]).max() <= LSE_MAX, f"head {h} LSE"
+        err_sum += err.sum()
+        sig_sum += sig.sum()
+        ref_sum += np.abs(o_ref).sum()
+    n = O.size
+    assert err_sum / n <= sig_sum / n + 2.0 ** -9 * ref_sum / n + 1e-5
