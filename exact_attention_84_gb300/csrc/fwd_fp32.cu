@@ -44,19 +44,54 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
                                                        float* __restrict__ lse, int N,
                                                        float scale, int causal) {
   constexpr int D = DL * 32;
-  __shared__ float sQ[kRowsPerBlock][D];
+  constexpr int D4 = D / 4;                      // float4 per row
+  constexpr int V4 = kKeysPerTile * D4 / 128;    // float4 of K (and of V) per thread per tile
+  __shared__ __align__(16) float sQ[kRowsPerBlock][D];
   __shared__ float sK[kKeysPerTile][D + 1];   // +1: lane j reads row j conflict-free
-  __shared__ float sV[kKeysPerTile][D];
+  __shared__ __align__(16) float sV[kKeysPerTile][D];
 
   const int bh = blockIdx.y;
   const int q0 = blockIdx.x * kRowsPerBlock;
   const size_t head = static_cast<size_t>(bh) * N * D;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float4* q4 = reinterpret_cast<const float4*>(q + head);
+  const float4* k4 = reinterpret_cast<const float4*>(k + head);
+  const float4* v4 = reinterpret_cast<const float4*>(v + head);
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  for (int idx = tid; idx < kRowsPerBlock * D; idx += blockDim.x) {
-    const int r = idx / D, c = idx % D;
-    sQ[r][c] = (q0 + r < N) ? q[head + static_cast<size_t>(q0 + r) * D + c] : 0.f;
+  for (int idx = tid; idx < kRowsPerBlock * D4; idx += blockDim.x) {
+    const int r = idx / D4, c = idx % D4;
+    *reinterpret_cast<float4*>(&sQ[r][4 * c]) =
+        (q0 + r < N) ? q4[static_cast<size_t>(q0 + r) * D4 + c] : zero4;
   }
+  // A K/V tile is fetched into registers with 16-byte loads, all issued
+  // before any is used, one tile ahead of its use, then stored to shared
+  // memory: the loads' latency is paid once per tile and hidden behind the
+  // previous tile's arithmetic.
+  float4 kr[V4], vr[V4];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < V4; ++i) {
+      const int idx = tid + 128 * i;             // float4 within the 32 x D tile
+      const int r = idx / D4, c = idx % D4;
+      const bool in = (k0 + r) < N;
+      const size_t g = static_cast<size_t>(k0 + r) * D4 + c;
+      kr[i] = in ? k4[g] : zero4;
+      vr[i] = in ? v4[g] : zero4;
+    }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int i = 0; i < V4; ++i) {
+      const int idx = tid + 128 * i;
+      const int r = idx / D4, c = 4 * (idx % D4);
+      sK[r][c] = kr[i].x;
+      sK[r][c + 1] = kr[i].y;
+      sK[r][c + 2] = kr[i].z;
+      sK[r][c + 3] = kr[i].w;
+      *reinterpret_cast<float4*>(&sV[r][c]) = vr[i];
+    }
+  };
 
   float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DL];
 #pragma unroll
@@ -69,16 +104,12 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const float* __restrict__
 
   // Keys beyond the last query row of this block are masked for every row.
   const int key_end = causal ? min(N, q0 + kRowsPerBlock) : N;
+  if (key_end > 0) fetch(0);
   for (int k0 = 0; k0 < key_end; k0 += kKeysPerTile) {
+    __syncthreads();                               // the previous tile has been read
+    stash();
     __syncthreads();
-    for (int idx = tid; idx < kKeysPerTile * D; idx += blockDim.x) {
-      const int r = idx / D, c = idx % D;
-      const bool in = (k0 + r) < N;
-      const size_t g = head + static_cast<size_t>(k0 + r) * D + c;
-      sK[r][c] = in ? k[g] : 0.f;
-      sV[r][c] = in ? v[g] : 0.f;
-    }
-    __syncthreads();
+    if (k0 + kKeysPerTile < key_end) fetch(k0 + kKeysPerTile);
 
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
