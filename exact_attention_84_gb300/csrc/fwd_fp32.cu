@@ -20,8 +20,8 @@ namespace {
 
 __device__ int g_status_fwd_fp32;   // no waits here; kept for a uniform status API
 
-constexpr int kRowsPerBlock = 8;    // 4 warps x 2 query rows
-constexpr int kRowsPerWarp = 2;
+constexpr int kRowsPerBlock = 4;    // 4 warps x 1 query row: 64 blocks on the tiny workload
+constexpr int kRowsPerWarp = 1;
 constexpr int kKeysPerTile = 32;    // one key per lane
 
 __device__ __forceinline__ float warp_max(float x) {
